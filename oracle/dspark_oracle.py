@@ -1,0 +1,280 @@
+"""Plain CPU oracle of the DSpark draft-and-schedule step (fp64, numpy).
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import it.
+The product path (the CUDA library and its Python binding) never does, and
+this module shares no code, table or helper with it.
+
+What it computes, step by step, with the passage each step follows:
+
+* Chaining ("DSpark on MAX", *What DSpark is*, item 3; "How DSpark Speeds Up
+  LLM Inference", *Draft better*): for every draft position k the backbone
+  logits are adjusted by a rank-r bias keyed on the previously chosen token,
+  bias[v] = U[prev] . V[v], and the token is the argmax of the adjusted row.
+  prev is the request's last committed token for k = 0, else the token just
+  chosen at k - 1.
+* Survival ("Adaptive Verification in vLLM", *Scheduling the budget*): the
+  running product of the confidences along each request.
+* Global top-B (same section): slots of all sampling requests compete on
+  survival; because survival only falls with position the best B slots form
+  a contiguous prefix of every request.
+* Budget (same section, the paragraph after the formula): B maximises
+  (N_sampling + sum of the best B survivals) / cost[T + B], an argmax over a
+  cumulative sum; T counts the step's non-draft tokens.
+* Cost table (same page, *The cost model*): profiled step costs in
+  microseconds, forced monotone; a drafter cost may be added.
+* Allocation and compaction (same page, *Scheduling the budget*; "How DSpark
+  Speeds Up LLM Inference", appendix Part B): each request gets its selected
+  prefix; the verify list is flattened across requests with per-request
+  offsets.
+
+Readings of points the pages leave open: exact cumulative sums (rounded
+once), first-index argmax with NaN ranked highest, slot ties broken by slot
+id, running-max forcing, b <= L-1-T, confidences clamped into [0, 1].
+
+Every function is pinned by ``tests/test_oracle_*.py`` against values and
+properties the pages and the mathematics fix (a worked instance, brute force
+over every slot subset, closed forms, exact integer arithmetic).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# device-status bits, mirrored from the C header's documented values so the
+# tests can compare flags; the numbers are part of the public contract
+TOKEN_OOR = 1
+NAN_LOGIT = 2
+CONF_OOR = 4
+TABLE_SHORT = 8
+COST_NONPOS = 16
+
+FORCE_RUNNING_MAX = 1
+FORCE_SUFFIX_MIN = 2
+BUDGET_GREEDY_STOP = 4
+
+
+# ---------------------------------------------------------------------------
+# inputs to fp64
+# ---------------------------------------------------------------------------
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact value of bf16 bit patterns (the upper half of an IEEE binary32)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
+    return bf16_to_f64(x) if dtype == "bf16" else np.asarray(x, np.float64)
+
+
+# ---------------------------------------------------------------------------
+# chaining
+# ---------------------------------------------------------------------------
+def markov_bias(U64: np.ndarray, V64: np.ndarray, prev: np.ndarray) -> np.ndarray:
+    """bias[n, v] = sum_j U[prev_n, j] * V[v, j]  (rank-r factorised head)."""
+    return U64[prev] @ V64.T
+
+
+def chain_position(logits_k64: np.ndarray, U64: np.ndarray, V64: np.ndarray,
+                   prev: np.ndarray) -> dict:
+    """One draft position: adjusted logits and their first-index argmax.
+
+    numpy's argmax returns the first maximal index and the first NaN if a row
+    holds one, which is the tie and NaN rule of the C ABI.
+    """
+    adj = logits_k64 + markov_bias(U64, V64, prev)
+    tok = np.argmax(adj, axis=1)
+    rows = np.arange(adj.shape[0])
+    best = adj[rows, tok]
+    # top-2 margin (for the near-tie tolerance of the parity tests)
+    if adj.shape[1] > 1:
+        part = np.partition(adj, adj.shape[1] - 2, axis=1)[:, -2:]
+        second = np.where(np.isnan(best), np.nan, part[:, 0])
+        top = np.where(np.isnan(best), np.nan, part[:, 1])
+        with np.errstate(invalid="ignore"):
+            margin = top - second
+    else:
+        margin = np.full(adj.shape[0], np.inf)
+    return dict(tok=tok.astype(np.int64), score=best, margin=margin,
+                absmax=np.abs(best), adj=adj)
+
+
+def chain(logits: np.ndarray, logits_dtype: str, U: np.ndarray, V: np.ndarray,
+          last_token: np.ndarray, keep_adj: bool = False) -> dict:
+    """Chain K draft positions for every row of ``logits`` [n, K, vocab].
+
+    U, V are bf16 bit patterns [vocab, rank].  Returns draft [n, K] (int64),
+    the adjusted value at the chosen token, the top-2 margin and |max| per
+    (row, position), and the status bits a device would raise.
+    """
+    U64 = bf16_to_f64(U)
+    V64 = bf16_to_f64(V)
+    n, K, vocab = logits.shape
+    status = 0
+    prev = np.asarray(last_token, dtype=np.int64).copy()
+    bad = (prev < 0) | (prev >= vocab)
+    if bad.any():
+        status |= TOKEN_OOR
+        prev[bad] = 0
+    draft = np.zeros((n, K), dtype=np.int64)
+    score = np.zeros((n, K))
+    margin = np.zeros((n, K))
+    absmax = np.zeros((n, K))
+    adjs = []
+    for k in range(K):
+        r = chain_position(to_f64(logits[:, k, :], logits_dtype), U64, V64, prev)
+        draft[:, k] = r["tok"]
+        score[:, k] = r["score"]
+        margin[:, k] = r["margin"]
+        absmax[:, k] = r["absmax"]
+        if np.isnan(r["score"]).any():
+            status |= NAN_LOGIT
+        if keep_adj:
+            adjs.append(r["adj"])
+        prev = r["tok"]
+    out = dict(draft=draft, score=score, margin=margin, absmax=absmax,
+               status=status)
+    if keep_adj:
+        out["adj"] = adjs
+    return out
+
+
+# ---------------------------------------------------------------------------
+# confidence-scheduled verification
+# ---------------------------------------------------------------------------
+def clamp_confidence(conf: np.ndarray):
+    """Confidences as fp64 in [0, 1]; NaN -> 0.  Returns (values, status)."""
+    c = np.asarray(conf, dtype=np.float64).copy()
+    status = 0
+    bad = np.isnan(c) | (c < 0.0) | (c > 1.0)
+    if bad.any():
+        status |= CONF_OOR
+    c[np.isnan(c)] = 0.0
+    c = np.minimum(np.maximum(c, 0.0), 1.0)
+    return c, status
+
+
+def survival(conf: np.ndarray, mask: np.ndarray):
+    """s[n, k] = prod_{j <= k} c[n, j], left to right; 0 for non-sampling rows."""
+    c, status = clamp_confidence(conf)
+    s = np.cumprod(c, axis=1)
+    s[np.asarray(mask) == 0, :] = 0.0
+    return s, status
+
+
+def order_slots(s: np.ndarray, mask: np.ndarray) -> np.ndarray:
+    """Eligible slots (rows of sampling requests) by survival desc, slot id asc."""
+    N, K = s.shape
+    slot = np.arange(N * K).reshape(N, K)
+    elig = np.repeat(np.asarray(mask) != 0, K).reshape(N, K)
+    ids = slot[elig]
+    vals = s[elig]
+    order = np.lexsort((ids, -vals))
+    return ids[order].astype(np.int64)
+
+
+def exact_prefix_sums(x: np.ndarray) -> np.ndarray:
+    """P_b = x_0 + ... + x_{b-1} for b = 0..len(x), each the exact sum rounded
+    once to the nearest double (ties to even).
+
+    Every double is an integer multiple of 2**-1074, so the running sum is
+    kept as a Python integer in those units and converted back with integer
+    true division, which Python rounds correctly.  The result does not depend
+    on the order of the additions.
+    """
+    out = np.empty(len(x) + 1, dtype=np.float64)
+    out[0] = 0.0
+    acc = 0
+    scale = 1 << 1074
+    for i, v in enumerate(np.asarray(x, dtype=np.float64).tolist()):
+        num, den = float(v).as_integer_ratio()
+        acc += num * (scale // den)
+        out[i + 1] = acc / scale
+    return out
+
+
+def force_monotone(cost: np.ndarray, mode: int = FORCE_RUNNING_MAX) -> np.ndarray:
+    """Cost table forced monotone non-decreasing.
+
+    FORCE_RUNNING_MAX: cost'[n] = max_{m <= n} cost[m].
+    FORCE_SUFFIX_MIN:  cost'[n] = min_{m >= n} cost[m] (a bigger, cheaper
+    graph bounds the cost of a smaller batch).  NaN propagates in both.
+    """
+    c = np.asarray(cost, dtype=np.float32)
+    if mode == FORCE_RUNNING_MAX:
+        return np.maximum.accumulate(c)
+    if mode == FORCE_SUFFIX_MIN:
+        return np.minimum.accumulate(c[::-1])[::-1].copy()
+    return c.copy()
+
+
+def budget(sorted_s: np.ndarray, n_sampling: int, cost: np.ndarray, T: int,
+           draft_cost: float = 0.0, greedy_stop: bool = False) -> dict:
+    """Verify budget B from the sorted survivals and a (forced) cost table.
+
+    f(b) = (N_sampling + P_b) / (cost[T + b] + draft_cost) for
+    b = 0..b_max, b_max = min(S, L - 1 - T); B = first argmax (NaN ranks
+    highest).  With greedy_stop, slots are admitted one at a time while f
+    strictly rises.  T outside [0, L) gives B = 0 and TABLE_SHORT.
+    """
+    cost = np.asarray(cost, dtype=np.float32)
+    L = len(cost)
+    S = len(sorted_s)
+    status = 0
+    if T < 0 or T >= L:
+        return dict(B=0, objective=0.0, b_max=0, P=np.zeros(1),
+                    f=np.zeros(1), status=TABLE_SHORT)
+    b_max = min(S, L - 1 - T)
+    P = exact_prefix_sums(np.asarray(sorted_s[:b_max], dtype=np.float64))
+    num = np.float64(n_sampling) + P
+    den = cost[T:T + b_max + 1].astype(np.float64) + np.float64(np.float32(draft_cost))
+    if not np.all(den > 0):
+        status |= COST_NONPOS
+    with np.errstate(divide="ignore", invalid="ignore"):
+        f = num / den
+    if greedy_stop:
+        B = 0
+        while B < b_max and f[B + 1] > f[B]:
+            B += 1
+    else:
+        B = int(np.argmax(f))
+    return dict(B=int(B), objective=float(f[B]), b_max=int(b_max), P=P, f=f,
+                status=status)
+
+
+def allocate(order: np.ndarray, B: int, N: int, K: int) -> np.ndarray:
+    """len[n] = number of request n's slots among the first B of the order."""
+    sel = np.asarray(order[:B], dtype=np.int64)
+    return np.bincount(sel // K, minlength=N).astype(np.int64)
+
+
+def compact(draft_len: np.ndarray, K: int, draft: np.ndarray | None = None) -> dict:
+    """Request-major flattened verify list: offsets, slot ids, draft tokens."""
+    draft_len = np.asarray(draft_len, dtype=np.int64)
+    cu = np.concatenate([[0], np.cumsum(draft_len)]).astype(np.int64)
+    parts = [n * K + np.arange(draft_len[n]) for n in range(len(draft_len))]
+    idx = np.concatenate(parts).astype(np.int64) if parts else np.zeros(0, np.int64)
+    tok = None if draft is None else np.asarray(draft).reshape(-1)[idx]
+    return dict(cu_len=cu, verify_idx=idx, verify_tok=tok)
+
+
+def select_step(conf, mask, cost, T, draft_cost=0.0, flags=0, draft=None) -> dict:
+    """Survival -> order -> budget -> allocation -> compaction in one call."""
+    conf = np.asarray(conf)
+    N, K = conf.shape
+    mask = np.ones(N, np.uint8) if mask is None else np.asarray(mask)
+    s, st = survival(conf, mask)
+    order = order_slots(s, mask)
+    mode = (FORCE_RUNNING_MAX if flags & FORCE_RUNNING_MAX else
+            FORCE_SUFFIX_MIN if flags & FORCE_SUFFIX_MIN else 0)
+    cost_used = force_monotone(cost, mode)
+    n_s = int((mask != 0).sum())
+    bud = budget(s.reshape(-1)[order], n_s, cost_used, int(T), draft_cost,
+                 greedy_stop=bool(flags & BUDGET_GREEDY_STOP))
+    ln = allocate(order, bud["B"], N, K)
+    cp = compact(ln, K, draft)
+    return dict(survival=s, order=order, n_sampling=n_s, n_eligible=len(order),
+                prefix=exact_prefix_sums(s.reshape(-1)[order]),
+                B=bud["B"], objective=bud["objective"], b_max=bud["b_max"],
+                f=bud["f"], draft_len=ln, cu_len=cp["cu_len"],
+                verify_idx=cp["verify_idx"], verify_tok=cp["verify_tok"],
+                cost_used=cost_used, status=st | bud["status"])

@@ -1,0 +1,93 @@
+"""Pins of the scheduler oracle on hand-worked instances (tests/golden/).
+
+W1 follows the vLLM blog's Figure 1 caption ("Adaptive Verification in
+vLLM", *Scheduling the budget*): 3 requests x 7 slots, best B = 11.
+W2 is built with exact binary values so that a wrong cost index, a wrong
+N_sampling or an eligible prefill request each changes B.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+def test_w1_fig1_best_b_is_11():
+    g = _load("w1_fig1_b11.json")
+    d = workloads.w1_instance()
+    np.testing.assert_array_equal(d["conf"], np.array(g["conf"], np.float32))
+    r = oracle.select_step(d["conf"], d["mask"], d["cost"], d["T"])
+    e = g["expected"]
+    assert r["B"] == e["B"]
+    assert r["draft_len"].tolist() == e["draft_len"]
+    assert r["cu_len"].tolist() == e["cu_len"]
+    assert r["verify_idx"].tolist() == e["verify_idx"]
+    assert r["order"][:12].tolist() == e["first_sorted"]
+    tol = g["rel_tol_values"]
+    assert r["prefix"][11] == pytest.approx(e["P_11"], rel=tol)
+    for b in (10, 11, 12):
+        assert r["f"][b] == pytest.approx(e[f"f_{b}"], rel=tol)
+    # B is the unique maximiser
+    f = r["f"]
+    assert np.sum(f == f.max()) == 1
+
+
+def test_w2_cost_index_and_sampling_count():
+    g = _load("w2_cost_index.json")
+    conf = np.array(g["conf"], np.float32)
+    mask = np.array(g["mask"], np.uint8)
+    cost = np.array(g["cost"], np.float32)
+    r = oracle.select_step(conf, mask, cost, g["T"])
+    e = g["expected"]
+    assert r["n_sampling"] == e["n_sampling"]
+    assert r["order"].tolist() == e["order"]
+    assert r["B"] == e["B"]
+    # every f value is exact in binary except 3/4.3125 and 3.25/6, which are
+    # single correctly-rounded divisions
+    np.testing.assert_array_equal(r["f"], np.array(e["f"]))
+    assert r["draft_len"].tolist() == e["draft_len"]
+    assert r["cu_len"].tolist() == e["cu_len"]
+    assert r["verify_idx"].tolist() == e["verify_idx"]
+
+
+def test_w2_mistakes_would_change_b():
+    """The instance discriminates the readings it is meant to pin."""
+    g = _load("w2_cost_index.json")
+    cost = np.array(g["cost"], np.float64)
+    s_sorted = np.array([0.5, 0.25, 0.25, 0.25])
+    P = np.concatenate([[0.0], np.cumsum(s_sorted)])
+
+    def best(ns, shift):
+        T = g["T"]
+        bmax = min(4, g["L"] - 1 - T - max(shift, 0))
+        f = [(ns + P[b]) / cost[T + b + shift] for b in range(bmax + 1)]
+        return int(np.argmax(f))
+
+    assert best(2, 0) == 3
+    assert best(2, -1) != 3
+    assert best(2, +1) != 3
+    assert best(3, 0) != 3
+
+
+def test_table_edges():
+    d = workloads.w1_instance()
+    L = len(d["cost"])
+    r = oracle.select_step(d["conf"], d["mask"], d["cost"], L - 1)
+    assert r["B"] == 0 and r["b_max"] == 0 and r["status"] == 0
+    r = oracle.select_step(d["conf"], d["mask"], d["cost"], L)
+    assert r["B"] == 0 and r["status"] & oracle.TABLE_SHORT
+    r = oracle.select_step(d["conf"], d["mask"], d["cost"], -1)
+    assert r["B"] == 0 and r["status"] & oracle.TABLE_SHORT
+    # b_max clipped by the table, not by the slots
+    r = oracle.select_step(d["conf"], d["mask"], d["cost"], L - 5)
+    assert r["b_max"] == 4 and r["B"] <= 4
