@@ -1,0 +1,235 @@
+/*
+ * dspark.h - C ABI of the DSpark draft-and-schedule step for NVIDIA GB300
+ * (sm_103a).  One shared library, libdspark.so.
+ *
+ * The step has two stages.
+ *
+ *   Chaining  ("DSpark on MAX", section "What DSpark is", item 3; "How DSpark
+ *   Speeds Up LLM Inference", section "Draft better"): a parallel drafter
+ *   emits backbone logits for K draft positions at once; a rank-r Markov
+ *   head adjusts position k's logits by bias[v] = U[prev] . V[v], prev being
+ *   the token chosen at k-1 (the request's last committed token at k = 0),
+ *   and an argmax over the vocabulary picks the token.
+ *
+ *   Confidence-scheduled verification ("Adaptive Verification in vLLM",
+ *   sections "Scheduling the budget" and "The cost model"): survival is the
+ *   running product of the per-position confidences; the best B slots over
+ *   all requests are verified, B maximising
+ *       (N_sampling + sum of the best B survivals) / cost[T + B]
+ *   over a profiled step-cost table forced monotone; every request receives
+ *   a contiguous prefix of its draft and the verify list is flattened across
+ *   requests with per-request offsets ("How DSpark Speeds Up LLM Inference",
+ *   appendix Part B: tokens flattened across requests plus a marker tensor).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is caller-owned memory.  Unless stated otherwise
+ *     it is DEVICE memory of the current CUDA device.  The library never
+ *     allocates, frees or synchronises, and copies to the host only in
+ *     dspark_read_status().  Every call is asynchronous on `stream` (a
+ *     cudaStream_t; NULL = legacy default stream).
+ *   - Arguments are validated on the host before anything is launched; a
+ *     failed check returns DSPARK_ERR_INVALID_ARG or DSPARK_ERR_UNSUPPORTED
+ *     and launches nothing.  A launch error returns DSPARK_ERR_CUDA.
+ *   - Data anomalies found on the device never trap: the kernel writes a
+ *     defined value and ORs a DSPARK_DEV_* bit into a uint32 status word that
+ *     lives at offset 0 of the caller's workspace.  The word is sticky: it is
+ *     cleared only by dspark_clear_status().  A workspace must be zero-filled
+ *     once before its first use.
+ *   - Every wait inside a kernel is bounded (about one second); a wait that
+ *     gives up sets DSPARK_DEV_TIMEOUT and the kernel returns.
+ *   - Calls that share a workspace must not overlap on the GPU.
+ *   - Index arrays are int32; slot ids are n*K + k.
+ */
+#ifndef DSPARK_H_
+#define DSPARK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DSPARK_API __attribute__((visibility("default")))
+#else
+#define DSPARK_API
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers */
+typedef struct CUstream_st *dspark_stream_t;
+
+typedef int32_t dspark_status;
+#define DSPARK_OK              0
+#define DSPARK_ERR_INVALID_ARG 1   /* NULL pointer, bad size, stride or alignment */
+#define DSPARK_ERR_UNSUPPORTED 2   /* valid but outside what this build handles */
+#define DSPARK_ERR_CUDA        3   /* a CUDA call or launch failed */
+#define DSPARK_ERR_WORKSPACE   4   /* workspace NULL or smaller than required */
+
+/* logits element types */
+#define DSPARK_BF16 0
+#define DSPARK_F32  1
+
+/* device status bits (status word at offset 0 of a workspace) */
+#define DSPARK_DEV_TOKEN_OOR   1u   /* last_token outside [0, vocab): 0 used instead */
+#define DSPARK_DEV_NAN_LOGIT   2u   /* an adjusted logit was NaN; it won its row */
+#define DSPARK_DEV_CONF_OOR    4u   /* confidence NaN or outside [0,1]: clamped, NaN -> 0 */
+#define DSPARK_DEV_TABLE_SHORT 8u   /* T outside [0, cost_len): B = 0 */
+#define DSPARK_DEV_COST_NONPOS 16u  /* a cost (+ draft_cost) in use was <= 0 or NaN */
+#define DSPARK_DEV_TIMEOUT     32u  /* a bounded wait gave up; outputs undefined */
+
+/* scheduler flags */
+#define DSPARK_COST_FORCE_MONOTONE   1u  /* use cost'[n] = max_{m<=n} cost[m] */
+#define DSPARK_COST_FORCE_SUFFIX_MIN 2u  /* use cost'[n] = min_{m>=n} cost[m] */
+#define DSPARK_BUDGET_GREEDY_STOP    4u  /* admit slots while the objective strictly rises */
+
+/* ------------------------------------------------------------------------
+ * Chaining.  "DSpark on MAX", "What DSpark is", item 3: a low-rank bias keyed
+ * on the previous chosen token, then an argmax.
+ *
+ * logits       [N, K, vocab] of logits_dtype; element (n, k, v) at
+ *              n*stride_n + k*stride_k + v (elements).  vocab, stride_n and
+ *              stride_k must be multiples of 16 bytes / element size, and
+ *              the base 16-byte aligned.
+ * U, V         bf16 [vocab, rank] row-major each, 16-byte aligned.
+ * last_token   [N] int32: the token before draft position 0.  Values outside
+ *              [0, vocab) are replaced by 0 and flag DSPARK_DEV_TOKEN_OOR.
+ * draft_tokens out [N, K] int32, row-major.  draft[n,k] is the first index of
+ *              the maximum of logits[n,k,:] + U[prev] . V^T (fp32 arithmetic,
+ *              bf16 products accumulated in fp32); a NaN ranks above every
+ *              number, so the first NaN wins and DSPARK_DEV_NAN_LOGIT is set.
+ *              An index outside [0, vocab) is never written.
+ * draft_score  optional out [N, K] fp32: the adjusted value at draft[n,k];
+ *              NULL to skip.
+ * workspace    >= dspark_chain_workspace_size(N, K) bytes, 256-byte aligned,
+ *              zero-filled before its first use.
+ * Limits: 1 <= N <= 128 * (SM count), 1 <= K <= 32, 8 <= vocab < 2^31,
+ * rank a multiple of 16 in [16, 256].
+ * ------------------------------------------------------------------------ */
+DSPARK_API size_t dspark_chain_workspace_size(int32_t N, int32_t K);
+
+DSPARK_API dspark_status dspark_chain_draft(
+    const void *logits, int32_t logits_dtype,
+    int64_t logits_stride_n, int64_t logits_stride_k,
+    const void *U, const void *V,
+    const int32_t *last_token,
+    int32_t N, int32_t K, int32_t vocab, int32_t rank,
+    int32_t *draft_tokens, float *draft_score,
+    void *workspace, size_t workspace_bytes, dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Scheduler workspace: dspark_select_workspace_size() bytes, 256-byte
+ * aligned, zero-filled before first use (status word at offset 0).
+ * Limits of every scheduler call: 1 <= N, 1 <= K <= 32, N*K <= 16384,
+ * 1 <= cost_len <= 2^30.
+ * ------------------------------------------------------------------------ */
+DSPARK_API size_t dspark_select_workspace_size(int32_t N, int32_t K, int32_t cost_len);
+
+/* Survival and global order.  "Adaptive Verification in vLLM", "Scheduling
+ * the budget": survival is the running product of confidences along each
+ * request; slots compete globally on it.
+ *
+ * conf          [N, K] fp32.  Clamped into [0,1] (NaN -> 0, DSPARK_DEV_CONF_OOR).
+ * sampling_mask [N] uint8, 1 = request samples this step; NULL = all sample.
+ * survival      out [N, K] fp32: prod_{j<=k} conf[n,j] computed left to right
+ *               in fp64 and rounded once; 0 for non-sampling requests.
+ * sorted_slots  out [N*K] int32: the S = N_sampling*K eligible slot ids by
+ *               survival descending, slot id ascending on ties; entries past S
+ *               are left untouched.
+ * prefix_sum    out [N*K+1] fp64: prefix_sum[b] = the exact sum of the first b
+ *               sorted survivals (as fp64 values) rounded once to fp64, for
+ *               b = 0..S.
+ * n_eligible    out device scalar: S.   n_sampling out device scalar.
+ */
+DSPARK_API dspark_status dspark_survival_topb(
+    const float *conf, const uint8_t *sampling_mask, int32_t N, int32_t K,
+    float *survival, int32_t *sorted_slots, double *prefix_sum,
+    int32_t *n_eligible, int32_t *n_sampling,
+    void *workspace, size_t workspace_bytes, dspark_stream_t stream);
+
+/* Budget.  "Adaptive Verification in vLLM", "Scheduling the budget" (the
+ * paragraph after the formula) and "The cost model".
+ *
+ * prefix_sum, n_eligible, n_sampling: as written by dspark_survival_topb.
+ * cost      [cost_len] fp32 microseconds, indexed by the step's token count.
+ * T_dev     device scalar: tokens of the step that are not drafts.
+ * draft_cost  host fp32 added to every cost (the drafter table's entry).
+ * flags     DSPARK_COST_FORCE_* (forcing applied on the fly, the table is not
+ *           written) and DSPARK_BUDGET_GREEDY_STOP.
+ * B         out device scalar: for b = 0..b_max, b_max = min(S, cost_len-1-T),
+ *           f(b) = fl(fl(N_sampling + prefix_sum[b]) / fl(cost'[T+b] + draft_cost))
+ *           in fp64; B is the first maximiser (NaN ranks highest).  T outside
+ *           [0, cost_len) gives B = 0 and DSPARK_DEV_TABLE_SHORT.
+ * objective out device scalar fp64: f(B) (0 when the table is short).
+ */
+DSPARK_API dspark_status dspark_choose_budget(
+    const double *prefix_sum, const int32_t *n_eligible,
+    const int32_t *n_sampling, const float *cost, int32_t cost_len,
+    const int32_t *T_dev, float draft_cost, uint32_t flags,
+    int32_t *B, double *objective,
+    void *workspace, size_t workspace_bytes, dspark_stream_t stream);
+
+/* Allocation.  "Adaptive Verification in vLLM", "Scheduling the budget": the
+ * B best slots give every request a contiguous prefix of its draft.
+ * draft_len out [N] int32: number of request n's slots among sorted_slots[0..B).
+ */
+DSPARK_API dspark_status dspark_allocate_prefix(
+    const int32_t *sorted_slots, const int32_t *B, int32_t N, int32_t K,
+    int32_t *draft_len,
+    void *workspace, size_t workspace_bytes, dspark_stream_t stream);
+
+/* Compaction.  "How DSpark Speeds Up LLM Inference", appendix Part B; "Adaptive
+ * Verification in vLLM", "Limitations" (logits compacted after the forward).
+ * cu_len     out [N+1] int32: exclusive prefix sum of draft_len (the marker).
+ * verify_idx out [N*K] int32: slot ids n*K+k for k < draft_len[n], request-
+ *            major; the first cu_len[N] entries are written.
+ * verify_tok optional out [N*K] int32: draft_tokens[verify_idx[j]]; needs
+ *            draft_tokens [N, K]; either may be NULL (then nothing is written).
+ */
+DSPARK_API dspark_status dspark_compact_verify(
+    const int32_t *draft_len, const int32_t *draft_tokens, int32_t N, int32_t K,
+    int32_t *cu_len, int32_t *verify_idx, int32_t *verify_tok,
+    void *workspace, size_t workspace_bytes, dspark_stream_t stream);
+
+/* The four scheduler calls above fused into one single-CTA launch that keeps
+ * every intermediate on chip and never reads back to the host ("Adaptive
+ * Verification in vLLM", "Scheduling the budget", last paragraph).  Outputs
+ * are identical to the four calls in sequence; any of survival, sorted_slots,
+ * prefix_sum, n_eligible, n_sampling, objective, verify_tok may be NULL. */
+DSPARK_API dspark_status dspark_select_step(
+    const float *conf, const uint8_t *sampling_mask, int32_t N, int32_t K,
+    const float *cost, int32_t cost_len, const int32_t *T_dev,
+    float draft_cost, uint32_t flags, const int32_t *draft_tokens,
+    float *survival, int32_t *sorted_slots, double *prefix_sum,
+    int32_t *n_eligible, int32_t *n_sampling,
+    int32_t *B, double *objective,
+    int32_t *draft_len, int32_t *cu_len, int32_t *verify_idx,
+    int32_t *verify_tok,
+    void *workspace, size_t workspace_bytes, dspark_stream_t stream);
+
+/* Cost-table preparation.  "Adaptive Verification in vLLM", "The cost model":
+ * profiling noise is removed by forcing the curve monotone; run once per
+ * table.  mode = DSPARK_COST_FORCE_MONOTONE (running max from the left) or
+ * DSPARK_COST_FORCE_SUFFIX_MIN (running min from the right); NaN propagates.
+ * cost_in and cost_out may alias. */
+DSPARK_API dspark_status dspark_force_monotone(
+    const float *cost_in, float *cost_out, int32_t cost_len, uint32_t mode,
+    dspark_stream_t stream);
+
+/* Copies the workspace's status word to *host_out (host memory) and waits
+ * for the copy; the only call that synchronises. */
+DSPARK_API dspark_status dspark_read_status(const void *workspace, uint32_t *host_out,
+                                 dspark_stream_t stream);
+
+/* Zeroes the workspace's status word (asynchronous). */
+DSPARK_API dspark_status dspark_clear_status(void *workspace, dspark_stream_t stream);
+
+/* Number of SMs the library plans its grids for (device attribute), and the
+ * library's version as major*10000 + minor*100 + patch. */
+DSPARK_API int32_t dspark_sm_count(void);
+DSPARK_API int32_t dspark_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSPARK_H_ */

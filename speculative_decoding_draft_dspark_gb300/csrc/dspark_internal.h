@@ -1,0 +1,81 @@
+// Internal interfaces between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+// workspace layout (bytes from the workspace base)
+constexpr size_t kStatusOffset = 0;         // uint32 sticky status word
+constexpr size_t kChainCounterOffset = 64;  // uint32 [K <= 32] CTA counters
+constexpr size_t kChainSlotsOffset = 256;   // uint64 [K][N] per-row winners
+constexpr size_t kSelectWorkspaceBytes = 256;
+
+constexpr int kMaxK = 32;
+constexpr int kMaxSlots = 16384;  // N*K limit of the scheduler kernels
+
+int device_sm_count(int dev);
+
+struct ChainArgs {
+  const void *logits;
+  int32_t logits_dtype;
+  int64_t stride_n, stride_k;
+  const void *U, *V;
+  const int32_t *last_token;
+  int32_t N, K, vocab, rank;
+  int32_t *draft;
+  float *score;
+  void *workspace;
+};
+size_t chain_workspace_bytes(int32_t N, int32_t K);
+dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream);
+
+struct SelectArgs {
+  const float *conf;
+  const uint8_t *mask;
+  int32_t N, K;
+  const float *cost;
+  int32_t L;
+  const int32_t *T_dev;
+  float draft_cost;
+  uint32_t flags;
+  const int32_t *draft;
+  // stage inputs for the separate calls
+  const double *prefix_in;
+  const int32_t *n_eligible_in;
+  const int32_t *n_sampling_in;
+  const int32_t *sorted_in;
+  const int32_t *B_in;
+  const int32_t *len_in;
+  // outputs (any may be NULL where the header allows)
+  float *survival;
+  int32_t *sorted_slots;
+  double *prefix_sum;
+  int32_t *n_eligible;
+  int32_t *n_sampling;
+  int32_t *B;
+  double *objective;
+  int32_t *draft_len;
+  int32_t *cu_len;
+  int32_t *verify_idx;
+  int32_t *verify_tok;
+  uint32_t *status;
+};
+
+enum SelectStage : uint32_t {
+  kStageSurvival = 1u,  // survival, order, exact prefix sums
+  kStageBudget = 2u,    // budget argmax
+  kStageAllocate = 4u,  // per-request prefix lengths
+  kStageCompact = 8u,   // offsets and the flattened verify list
+};
+
+dspark_status select_launch(const SelectArgs &a, uint32_t stages,
+                            cudaStream_t stream);
+dspark_status force_monotone_launch(const float *in, float *out, int32_t L,
+                                    uint32_t mode, cudaStream_t stream);
+
+}  // namespace dspark

@@ -1,0 +1,706 @@
+// Confidence-scheduled verification on sm_103a: one persistent CTA.
+//
+// "Adaptive Verification in vLLM", section "Scheduling the budget":
+//   survival  s[n,k] = prod_{j<=k} c[n,j]                 (running product)
+//   order     every sampling request's slots by survival  (global top-B)
+//   budget    B = argmax_b (N_sampling + P_b) / cost[T+b], P_b the sum of
+//             the b best survivals ("an np.argmax over a cumulative sum")
+//   allocate  each request keeps the contiguous prefix of its selected slots
+//   compact   flattened verify list with per-request offsets
+// and section "The cost model": the cost table is forced monotone.  The
+// whole selection runs on the GPU and never reads back to the host.
+//
+// Numerics: survivals are fp64 products taken left to right (each one IEEE
+// multiply), sort keys are their bit patterns, and P_b is the exact sum of
+// the first b survivals rounded once, computed as a 256-bit fixed-point
+// prefix scan (integer addition is associative, so the parallel scan gives
+// the same bits as any order).  f(b) is then one fp64 add and one fp64
+// divide.  B is therefore decided on exactly the values the definition
+// names.
+//
+// The kernel runs the stages requested by a mask, so the fused call and the
+// four separate calls share one implementation.
+#include <climits>
+#include <mutex>
+
+#include "common.cuh"
+#include "dspark_internal.h"
+
+namespace dspark {
+
+constexpr int SEL_THREADS = 1024;
+constexpr int SEL_WARPS = SEL_THREADS / 32;
+constexpr unsigned FULL = 0xFFFFFFFFu;
+
+// ------------------------------------------------------------------------
+// 256-bit fixed-point accumulator for exact sums of non-negative doubles
+// ------------------------------------------------------------------------
+// Every term s is written as an integer X = s * 2^-u with the unit
+// u = e_max - 1075 - kFixG, e_max being the biased exponent of the largest
+// term: the largest term occupies bits [kFixG, kFixG + 53) and a sum of up
+// to 2^14 terms stays below bit 256.  Bits of terms smaller than 2^-kFixG
+// times the largest fall below the unit; they are folded into a sticky bit,
+// which keeps the final rounding exact (they cannot reach the rounding
+// position, kFixG - 53 bits above the unit).
+constexpr int kFixG = 188;
+
+struct Acc256 {
+  unsigned long long w0, w1, w2, w3;
+  uint32_t sticky;
+};
+
+__device__ __forceinline__ Acc256 acc_zero() { return Acc256{0, 0, 0, 0, 0}; }
+
+__device__ __forceinline__ void acc_add(Acc256 &a, const Acc256 &b) {
+  asm("add.cc.u64 %0, %0, %4;\n\t"
+      "addc.cc.u64 %1, %1, %5;\n\t"
+      "addc.cc.u64 %2, %2, %6;\n\t"
+      "addc.u64 %3, %3, %7;"
+      : "+l"(a.w0), "+l"(a.w1), "+l"(a.w2), "+l"(a.w3)
+      : "l"(b.w0), "l"(b.w1), "l"(b.w2), "l"(b.w3));
+  a.sticky |= b.sticky;
+}
+
+__device__ __forceinline__ unsigned long long acc_word(const Acc256 &a, int i) {
+  return i == 0 ? a.w0 : i == 1 ? a.w1 : i == 2 ? a.w2 : i == 3 ? a.w3 : 0ull;
+}
+
+// m * 2^shift restricted to word i (bits [64 i, 64 i + 64)), m < 2^53
+__device__ __forceinline__ unsigned long long shifted_word(unsigned long long m,
+                                                           int shift, int i) {
+  const int d = shift - 64 * i;
+  if (d >= 0 && d < 64) return m << d;
+  if (d < 0 && d > -64) return m >> (-d);
+  return 0ull;
+}
+
+__device__ __forceinline__ Acc256 to_fixed(double s, int e_max) {
+  Acc256 r = acc_zero();
+  const unsigned long long bits =
+      static_cast<unsigned long long>(__double_as_longlong(s));
+  int ex = static_cast<int>((bits >> 52) & 0x7FF);
+  unsigned long long m = bits & 0xFFFFFFFFFFFFFull;
+  if (ex == 0)
+    ex = 1;
+  else
+    m |= 1ull << 52;
+  if (m == 0ull) return r;
+  const int shift = ex - e_max + kFixG;
+  if (shift >= 0) {
+    r.w0 = shifted_word(m, shift, 0);
+    r.w1 = shifted_word(m, shift, 1);
+    r.w2 = shifted_word(m, shift, 2);
+    r.w3 = shifted_word(m, shift, 3);
+  } else if (shift > -53) {
+    const int sh = -shift;
+    r.w0 = m >> sh;
+    r.sticky = (m & ((1ull << sh) - 1ull)) != 0ull;
+  } else {
+    r.sticky = 1u;
+  }
+  return r;
+}
+
+__device__ __forceinline__ uint32_t acc_bit(const Acc256 &a, int pos) {
+  return static_cast<uint32_t>((acc_word(a, pos >> 6) >> (pos & 63)) & 1ull);
+}
+
+// any of the bits [0, pos) set
+__device__ __forceinline__ bool acc_any_below(const Acc256 &a, int pos) {
+  if (pos <= 0) return false;
+  const int wi = pos >> 6, bi = pos & 63;
+  bool any = false;
+  if (wi > 0) any |= a.w0 != 0ull;
+  if (wi > 1) any |= a.w1 != 0ull;
+  if (wi > 2) any |= a.w2 != 0ull;
+  if (wi > 3) any |= a.w3 != 0ull;
+  if (bi != 0 && wi < 4) any |= (acc_word(a, wi) & ((1ull << bi) - 1ull)) != 0ull;
+  return any;
+}
+
+// bits [pos, pos + 53) of a, pos >= 0
+__device__ __forceinline__ unsigned long long acc_extract53(const Acc256 &a,
+                                                             int pos) {
+  const int wi = pos >> 6, bi = pos & 63;
+  unsigned long long v = acc_word(a, wi) >> bi;
+  if (bi != 0) v |= acc_word(a, wi + 1) << (64 - bi);
+  return v & ((1ull << 53) - 1ull);
+}
+
+// a * 2^u rounded to the nearest double, ties to even
+__device__ __forceinline__ double from_fixed(const Acc256 &a, int e_max) {
+  int h = -1;
+  if (a.w3)
+    h = 192 + 63 - __clzll(static_cast<long long>(a.w3));
+  else if (a.w2)
+    h = 128 + 63 - __clzll(static_cast<long long>(a.w2));
+  else if (a.w1)
+    h = 64 + 63 - __clzll(static_cast<long long>(a.w1));
+  else if (a.w0)
+    h = 63 - __clzll(static_cast<long long>(a.w0));
+  if (h < 0) return 0.0;
+  const int u = e_max - 1075 - kFixG;
+  int rb = h - 52;                 // lowest bit a 53-bit significand keeps
+  const int rb_sub = -1074 - u;    // lowest bit a subnormal keeps
+  if (rb < rb_sub) rb = rb_sub;
+  if (rb < 0) rb = 0;              // whole value fits: exact
+  unsigned long long mant = acc_extract53(a, rb);
+  const bool round = rb >= 1 && acc_bit(a, rb - 1);
+  const bool sticky = a.sticky != 0u || acc_any_below(a, rb - 1);
+  if (round && (sticky || (mant & 1ull))) mant += 1ull;
+  int e2 = rb + u;                 // value = mant * 2^e2
+  if (mant == (1ull << 53)) {
+    mant >>= 1;
+    e2 += 1;
+  }
+  unsigned long long bits;
+  if (mant >= (1ull << 52))
+    bits = (static_cast<unsigned long long>(e2 + 52 + 1023) << 52) |
+           (mant & ((1ull << 52) - 1ull));
+  else
+    bits = mant;  // subnormal, e2 == -1074
+  return __longlong_as_double(static_cast<long long>(bits));
+}
+
+// ------------------------------------------------------------------------
+// block-level scans and reductions (blockDim = SEL_THREADS)
+// ------------------------------------------------------------------------
+__device__ __forceinline__ int shfl_up(int v, int o) { return __shfl_up_sync(FULL, v, o); }
+__device__ __forceinline__ float shfl_up(float v, int o) { return __shfl_up_sync(FULL, v, o); }
+__device__ __forceinline__ float shfl_down(float v, int o) { return __shfl_down_sync(FULL, v, o); }
+__device__ __forceinline__ Acc256 shfl_up(const Acc256 &v, int o) {
+  Acc256 r;
+  r.w0 = __shfl_up_sync(FULL, v.w0, o);
+  r.w1 = __shfl_up_sync(FULL, v.w1, o);
+  r.w2 = __shfl_up_sync(FULL, v.w2, o);
+  r.w3 = __shfl_up_sync(FULL, v.w3, o);
+  r.sticky = __shfl_up_sync(FULL, v.sticky, o);
+  return r;
+}
+
+struct OpAddInt {
+  __device__ int operator()(int a, int b) const { return a + b; }
+};
+struct OpMaxNan {
+  __device__ float operator()(float a, float b) const { return fmax_nan(a, b); }
+};
+struct OpMinNan {
+  __device__ float operator()(float a, float b) const {
+    float d;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+  }
+};
+struct OpAcc {
+  __device__ Acc256 operator()(Acc256 a, const Acc256 &b) const {
+    acc_add(a, b);
+    return a;
+  }
+};
+
+// exclusive scan in thread order; `sh` holds SEL_WARPS + 1 values
+template <typename T, typename Op>
+__device__ T block_excl_scan(T v, Op op, T ident, T *sh, T *total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  T x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    T y = shfl_up(x, o);
+    if (lane >= o) x = op(y, x);
+  }
+  if (lane == 31) sh[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    T t = sh[lane];
+    T s = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      T y = shfl_up(s, o);
+      if (lane >= o) s = op(y, s);
+    }
+    T prev = shfl_up(s, 1);
+    sh[lane] = lane == 0 ? ident : prev;
+    if (lane == 31) sh[SEL_WARPS] = s;
+  }
+  __syncthreads();
+  T in_warp = shfl_up(x, 1);
+  if (lane == 0) in_warp = ident;
+  T r = op(sh[w], in_warp);
+  if (total) *total = sh[SEL_WARPS];
+  __syncthreads();
+  return r;
+}
+
+// exclusive scan in reverse thread order: op over the values of threads
+// tid+1 .. blockDim-1
+template <typename Op>
+__device__ float block_excl_scan_rev(float v, Op op, float ident, float *sh) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  float x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    float y = shfl_down(x, o);
+    if (lane + o < 32) x = op(x, y);
+  }
+  if (lane == 0) sh[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    float s = sh[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      float y = shfl_down(s, o);
+      if (lane + o < 32) s = op(s, y);
+    }
+    float next = shfl_down(s, 1);
+    sh[lane] = lane == 31 ? ident : next;
+  }
+  __syncthreads();
+  float in_warp = shfl_down(x, 1);
+  if (lane == 31) in_warp = ident;
+  const float r = op(in_warp, sh[w]);
+  __syncthreads();
+  return r;
+}
+
+template <typename T, typename Op>
+__device__ T block_reduce(T v, Op op, T ident, T *sh) {
+  T tot;
+  block_excl_scan(v, op, ident, sh, &tot);
+  return tot;
+}
+
+// argmax over (orderable key, index): larger key, then smaller index
+__device__ void block_argmax(unsigned long long &key, int &idx,
+                             unsigned long long *shk, int *shi) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long k2 = __shfl_down_sync(FULL, key, o);
+    const int i2 = __shfl_down_sync(FULL, idx, o);
+    if (k2 > key || (k2 == key && i2 < idx)) {
+      key = k2;
+      idx = i2;
+    }
+  }
+  if (lane == 0) {
+    shk[w] = key;
+    shi[w] = idx;
+  }
+  __syncthreads();
+  if (w == 0) {
+    key = shk[lane];
+    idx = shi[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long k2 = __shfl_down_sync(FULL, key, o);
+      const int i2 = __shfl_down_sync(FULL, idx, o);
+      if (k2 > key || (k2 == key && i2 < idx)) {
+        key = k2;
+        idx = i2;
+      }
+    }
+    if (lane == 0) {
+      shk[SEL_WARPS] = key;
+      shi[SEL_WARPS] = idx;
+    }
+  }
+  __syncthreads();
+  key = shk[SEL_WARPS];
+  idx = shi[SEL_WARPS];
+  __syncthreads();
+}
+
+// first index with value (smaller index wins), carrying a double payload
+__device__ void block_argmin_idx(int &idx, double &val, int *shi, double *shv) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const int i2 = __shfl_down_sync(FULL, idx, o);
+    const double v2 = __shfl_down_sync(FULL, val, o);
+    if (i2 < idx) {
+      idx = i2;
+      val = v2;
+    }
+  }
+  if (lane == 0) {
+    shi[w] = idx;
+    shv[w] = val;
+  }
+  __syncthreads();
+  if (w == 0) {
+    idx = shi[lane];
+    val = shv[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const int i2 = __shfl_down_sync(FULL, idx, o);
+      const double v2 = __shfl_down_sync(FULL, val, o);
+      if (i2 < idx) {
+        idx = i2;
+        val = v2;
+      }
+    }
+    if (lane == 0) {
+      shi[SEL_WARPS] = idx;
+      shv[SEL_WARPS] = val;
+    }
+  }
+  __syncthreads();
+  idx = shi[SEL_WARPS];
+  val = shv[SEL_WARPS];
+  __syncthreads();
+}
+
+__device__ __forceinline__ double key_value(unsigned long long key) {
+  return __longlong_as_double(static_cast<long long>(key - 1ull));
+}
+
+__device__ __forceinline__ double f64_from_key(unsigned long long k) {
+  if (k == 0xFFFFFFFFFFFFFFFFull)
+    return __longlong_as_double(0x7FF8000000000000ll);
+  const unsigned long long b =
+      (k & 0x8000000000000000ull) ? (k & 0x7FFFFFFFFFFFFFFFull) : ~k;
+  return __longlong_as_double(static_cast<long long>(b));
+}
+
+// ------------------------------------------------------------------------
+// the scheduler kernel
+// ------------------------------------------------------------------------
+constexpr int kMaxChunk = (kMaxSlots + 1 + SEL_THREADS - 1) / SEL_THREADS + 1;
+
+__global__ void __launch_bounds__(SEL_THREADS, 1)
+    select_kernel(const SelectArgs a, const uint32_t stages, const int P2) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  unsigned long long *keys = reinterpret_cast<unsigned long long *>(dsm);  // [P2+1]
+  uint16_t *sidx = reinterpret_cast<uint16_t *>(keys + P2 + 1);           // [P2]
+  double *Pd = reinterpret_cast<double *>(keys);  // after the scan: P_{j+1}
+  int *len_sm = reinterpret_cast<int *>(dsm);     // after the budget
+
+  __shared__ int sh_int[SEL_WARPS + 1];
+  __shared__ float sh_f[SEL_WARPS + 1];
+  __shared__ Acc256 sh_acc[SEL_WARPS + 1];
+  __shared__ unsigned long long sh_k[SEL_WARPS + 1];
+  __shared__ double sh_d[SEL_WARPS + 1];
+  __shared__ int sh_B;
+
+  const int tid = threadIdx.x;
+  const int NT = blockDim.x;
+  const int N = a.N, K = a.K, NK = N * K;
+  const bool fused_order = (stages & kStageSurvival) != 0;
+  int S = 0, n_s = 0;
+  uint32_t st = 0;
+
+  // ---------------------------------------------------- survival + order
+  if (stages & kStageSurvival) {
+    int my_ns = 0;
+    for (int n = tid; n < N; n += NT) {
+      const bool samp = a.mask == nullptr || a.mask[n] != 0;
+      my_ns += samp ? 1 : 0;
+      double prod = 1.0;
+      for (int k = 0; k < K; ++k) {
+        float c = a.conf[static_cast<size_t>(n) * K + k];
+        if (!(c >= 0.0f && c <= 1.0f)) {
+          st |= DSPARK_DEV_CONF_OOR;
+          c = (c > 1.0f) ? 1.0f : 0.0f;  // NaN and negatives -> 0
+        }
+        if (c == 0.0f) c = 0.0f;  // -0 -> +0: sort keys are bit patterns
+        prod = __dmul_rn(prod, static_cast<double>(c));
+        if (a.survival)
+          a.survival[static_cast<size_t>(n) * K + k] =
+              samp ? __double2float_rn(prod) : 0.0f;
+        keys[n * K + k] =
+            samp ? static_cast<unsigned long long>(__double_as_longlong(prod)) + 1ull
+                 : 0ull;
+        sidx[n * K + k] = static_cast<uint16_t>(n * K + k);
+      }
+    }
+    for (int i = NK + tid; i < P2; i += NT) {
+      keys[i] = 0ull;
+      sidx[i] = 0xFFFFu;
+    }
+    n_s = block_reduce(my_ns, OpAddInt(), 0, sh_int);
+    S = n_s * K;
+
+    // bitonic network: priority = larger key, then smaller slot id
+    for (int size = 2; size <= P2; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < (P2 >> 1); i += NT) {
+          const int lo = ((i & ~(stride - 1)) << 1) | (i & (stride - 1));
+          const int hi = lo + stride;
+          const unsigned long long ka = keys[lo], kb = keys[hi];
+          const uint16_t ia = sidx[lo], ib = sidx[hi];
+          const bool a_first = ka > kb || (ka == kb && ia < ib);
+          const bool up = (lo & size) == 0;
+          if (up != a_first) {
+            keys[lo] = kb;
+            keys[hi] = ka;
+            sidx[lo] = ib;
+            sidx[hi] = ia;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    if (a.sorted_slots)
+      for (int j = tid; j < S; j += NT) a.sorted_slots[j] = sidx[j];
+    if (tid == 0) {
+      if (a.n_eligible) *a.n_eligible = S;
+      if (a.n_sampling) *a.n_sampling = n_s;
+    }
+
+    // exact prefix sums of the sorted survivals
+    int e_max = 1;
+    if (S > 0) {
+      const int ex = static_cast<int>(((keys[0] - 1ull) >> 52) & 0x7FF);
+      e_max = ex == 0 ? 1 : ex;
+    }
+    const int C = (S + NT - 1) / NT;
+    const int j0 = min(S, tid * C), j1 = min(S, j0 + C);
+    Acc256 tot = acc_zero();
+    for (int j = j0; j < j1; ++j) acc_add(tot, to_fixed(key_value(keys[j]), e_max));
+    Acc256 run = block_excl_scan(tot, OpAcc(), acc_zero(), sh_acc,
+                                 static_cast<Acc256 *>(nullptr));
+    for (int j = j0; j < j1; ++j) {
+      acc_add(run, to_fixed(key_value(keys[j]), e_max));
+      const double P = from_fixed(run, e_max);
+      Pd[j] = P;  // this thread's own element: no other thread reads it
+      if (a.prefix_sum) a.prefix_sum[j + 1] = P;
+    }
+    if (tid == 0 && a.prefix_sum) a.prefix_sum[0] = 0.0;
+    __syncthreads();
+  } else if (stages & kStageBudget) {
+    S = *a.n_eligible_in;
+    n_s = *a.n_sampling_in;
+    if (S < 0) S = 0;
+    if (S > NK) S = NK;
+  }
+
+  // ---------------------------------------------------------------- budget
+  if (stages & kStageBudget) {
+    const int T = *a.T_dev;
+    const int L = a.L;
+    int B = 0;
+    double objective = 0.0;
+    if (T < 0 || T >= L) {
+      st |= DSPARK_DEV_TABLE_SHORT;
+    } else {
+      const int b_max = min(S, L - 1 - T);
+      const int nb = b_max + 1;
+      const int C2 = (nb + NT - 1) / NT;
+      const int b0 = min(nb, tid * C2), b1 = min(nb, b0 + C2);  // [b0, b1)
+      const bool has_next = b1 < nb && b1 > b0;                // f(b1) too
+      const float *cost = a.cost + T;
+      const int mode = (a.flags & DSPARK_COST_FORCE_MONOTONE)   ? 1
+                       : (a.flags & DSPARK_COST_FORCE_SUFFIX_MIN) ? 2
+                                                                 : 0;
+      float cf[kMaxChunk + 1];  // forced cost at b0 .. b1 (inclusive)
+      const int cnt = (b1 - b0) + (has_next ? 1 : 0);
+      if (mode == 1) {
+        float pre = -INFINITY;
+        for (int i = tid; i < T; i += NT) pre = fmax_nan(pre, a.cost[i]);
+        pre = block_reduce(pre, OpMaxNan(), -INFINITY, sh_f);
+        float loc = -INFINITY;
+        for (int b = b0; b < b1; ++b) loc = fmax_nan(loc, cost[b]);
+        float run = block_excl_scan(loc, OpMaxNan(), -INFINITY, sh_f,
+                                    static_cast<float *>(nullptr));
+        run = fmax_nan(run, pre);
+        for (int i = 0; i < cnt; ++i) {
+          run = fmax_nan(run, cost[b0 + i]);
+          cf[i] = run;
+        }
+      } else if (mode == 2) {
+        float post = INFINITY;
+        for (int i = T + nb + tid; i < L; i += NT) post = OpMinNan()(post, a.cost[i]);
+        post = block_reduce(post, OpMinNan(), INFINITY, sh_f);
+        float loc = INFINITY;
+        for (int b = b0; b < b1; ++b) loc = OpMinNan()(loc, cost[b]);
+        float run = block_excl_scan_rev(loc, OpMinNan(), INFINITY, sh_f);
+        run = OpMinNan()(run, post);  // min over cost[T+b1 ..]
+        if (has_next) cf[cnt - 1] = run;  // forced value at b1
+        for (int i = b1 - b0 - 1; i >= 0; --i) {
+          run = OpMinNan()(run, cost[b0 + i]);
+          cf[i] = run;
+        }
+      } else {
+        for (int i = 0; i < cnt; ++i) cf[i] = cost[b0 + i];
+      }
+      const double dc = static_cast<double>(a.draft_cost);
+      const double ns = static_cast<double>(n_s);
+      unsigned long long best_k = 0ull;
+      int best_b = INT_MAX;
+      int gstop = INT_MAX;
+      double gval = 0.0;
+      double f_prev = 0.0;
+      for (int i = 0; i < cnt; ++i) {
+        const int b = b0 + i;
+        double P;
+        if (b == 0)
+          P = 0.0;
+        else
+          P = fused_order ? Pd[b - 1] : a.prefix_in[b];
+        const double den = __dadd_rn(static_cast<double>(cf[i]), dc);
+        if (!(den > 0.0)) st |= DSPARK_DEV_COST_NONPOS;
+        const double f = __ddiv_rn(__dadd_rn(ns, P), den);
+        if (b < b1) {
+          const unsigned long long k = f64_key(f);
+          if (k > best_k || (k == best_k && b < best_b)) {
+            best_k = k;
+            best_b = b;
+          }
+        }
+        if (i > 0 && gstop == INT_MAX && !(f > f_prev)) {
+          gstop = b - 1;
+          gval = f_prev;
+        }
+        f_prev = f;
+      }
+      if (a.flags & DSPARK_BUDGET_GREEDY_STOP) {
+        // the objective at b_max for "never stopped"
+        if (b1 == nb && b1 > b0 && gstop == INT_MAX) {
+          gstop = INT_MAX - 1;  // marker: reached the end
+          gval = f_prev;
+        }
+        block_argmin_idx(gstop, gval, sh_int, sh_d);
+        B = (gstop >= INT_MAX - 1) ? b_max : gstop;
+        objective = gval;
+      } else {
+        block_argmax(best_k, best_b, sh_k, sh_int);
+        B = best_b;
+        objective = f64_from_key(best_k);
+      }
+    }
+    if (tid == 0) {
+      sh_B = B;
+      if (a.B) *a.B = B;
+      if (a.objective) *a.objective = objective;
+    }
+    __syncthreads();
+  } else if (stages & kStageAllocate) {
+    if (tid == 0) {
+      int B = *a.B_in;
+      sh_B = B < 0 ? 0 : (B > NK ? NK : B);
+    }
+    __syncthreads();
+  }
+
+  // -------------------------------------------------------------- allocate
+  if (stages & kStageAllocate) {
+    const int B = sh_B;
+    for (int n = tid; n < N; n += NT) len_sm[n] = 0;
+    __syncthreads();
+    for (int j = tid; j < B; j += NT) {
+      const int id = fused_order ? static_cast<int>(sidx[j]) : a.sorted_in[j];
+      if (id >= 0 && id < NK) atomicAdd(&len_sm[id / K], 1);
+    }
+    __syncthreads();
+    if (a.draft_len)
+      for (int n = tid; n < N; n += NT) a.draft_len[n] = len_sm[n];
+  }
+
+  // --------------------------------------------------------------- compact
+  if (stages & kStageCompact) {
+    const bool from_sm = (stages & kStageAllocate) != 0;
+    const int C3 = (N + NT - 1) / NT;
+    const int n0 = min(N, tid * C3), n1 = min(N, n0 + C3);
+    int loc = 0;
+    for (int n = n0; n < n1; ++n) {
+      int ln = from_sm ? len_sm[n] : a.len_in[n];
+      ln = ln < 0 ? 0 : (ln > K ? K : ln);
+      loc += ln;
+    }
+    int total = 0;
+    int off = block_excl_scan(loc, OpAddInt(), 0, sh_int, &total);
+    for (int n = n0; n < n1; ++n) {
+      int ln = from_sm ? len_sm[n] : a.len_in[n];
+      ln = ln < 0 ? 0 : (ln > K ? K : ln);
+      if (a.cu_len) a.cu_len[n] = off;
+      for (int k = 0; k < ln; ++k) {
+        const int idx = n * K + k;
+        if (a.verify_idx) a.verify_idx[off + k] = idx;
+        if (a.verify_tok && a.draft) a.verify_tok[off + k] = a.draft[idx];
+      }
+      off += ln;
+    }
+    if (tid == 0 && a.cu_len) a.cu_len[N] = total;
+  }
+
+  if (st) raise_status(a.status, st);
+}
+
+// forced cost table, one CTA: running max from the left or min from the right
+__global__ void __launch_bounds__(SEL_THREADS, 1)
+    force_monotone_kernel(const float *in, float *out, const int L,
+                          const uint32_t mode) {
+  __shared__ float sh_f[SEL_WARPS + 1];
+  const int tid = threadIdx.x, NT = blockDim.x;
+  const int C = (L + NT - 1) / NT;
+  const int i0 = min(L, tid * C), i1 = min(L, i0 + C);
+  if (mode == DSPARK_COST_FORCE_MONOTONE) {
+    float loc = -INFINITY;
+    for (int i = i0; i < i1; ++i) loc = fmax_nan(loc, in[i]);
+    float run = block_excl_scan(loc, OpMaxNan(), -INFINITY, sh_f,
+                                static_cast<float *>(nullptr));
+    for (int i = i0; i < i1; ++i) {
+      run = fmax_nan(run, in[i]);
+      out[i] = run;
+    }
+  } else {
+    float loc = INFINITY;
+    for (int i = i0; i < i1; ++i) loc = OpMinNan()(loc, in[i]);
+    float run = block_excl_scan_rev(loc, OpMinNan(), INFINITY, sh_f);
+    for (int i = i1 - 1; i >= i0; --i) {
+      run = OpMinNan()(run, in[i]);
+      out[i] = run;
+    }
+  }
+}
+
+// ==========================================================================
+// host side
+// ==========================================================================
+static std::mutex g_sel_mu;
+static bool g_sel_attr[128];
+
+static int next_pow2(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+dspark_status select_launch(const SelectArgs &a, uint32_t stages,
+                            cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128)
+    return DSPARK_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_sel_mu);
+    if (!g_sel_attr[dev]) {
+      if (cudaFuncSetAttribute(select_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               200 * 1024) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+      g_sel_attr[dev] = true;
+    }
+  }
+  const int NK = a.N * a.K;
+  int P2 = 0;
+  size_t dyn = 0;
+  if (stages & kStageSurvival) {
+    P2 = next_pow2(NK < 64 ? 64 : NK);
+    dyn = static_cast<size_t>(P2 + 1) * 8 + static_cast<size_t>(P2) * 2;
+  }
+  if (stages & kStageAllocate) {
+    const size_t need = static_cast<size_t>(a.N) * 4;
+    if (need > dyn) dyn = need;
+  }
+  dyn = (dyn + 15) & ~static_cast<size_t>(15);
+  select_kernel<<<1, SEL_THREADS, dyn, stream>>>(a, stages, P2);
+  return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+dspark_status force_monotone_launch(const float *in, float *out, int32_t L,
+                                    uint32_t mode, cudaStream_t stream) {
+  force_monotone_kernel<<<1, SEL_THREADS, 0, stream>>>(in, out, L, mode);
+  return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+}  // namespace dspark

@@ -1,0 +1,200 @@
+"""Helpers of the GPU parity tests: upload numpy inputs, call the C ABI
+through the Python binding, and compare with the oracle under the tolerance
+rules of the test plan.
+
+Chain tolerance: integer tokens must equal the oracle's, except where the
+oracle's top-2 margin is below 1e-3 * |max| (the adjusted values are fp32 on
+the device, fp64 in the oracle); there the device token must be within
+1e-3 * |max| of the maximum, and the rest of that row is checked for
+validity given the device's own earlier tokens.  Scores agree to 1e-5
+relative.  Scheduler outputs are compared bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from speculative_decoding_draft_dspark_gb300 import dspark as D
+
+DEV = "cuda:0"
+NEAR_TIE = 1e-3
+SCORE_RTOL = 1e-5
+
+
+def up(a) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def up_bf16(bits: np.ndarray) -> torch.Tensor:
+    return up(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def i32(n) -> torch.Tensor:
+    return torch.zeros(n, dtype=torch.int32, device=DEV)
+
+
+# --------------------------------------------------------------- chain
+def run_chain(logits: np.ndarray, dtype: str, U: np.ndarray, V: np.ndarray,
+              last: np.ndarray, layout: str = "nkv", pad: int = 0,
+              with_score: bool = True):
+    """Runs dspark_chain_draft; logits [N, K, vocab] stored in `layout`
+    ("nkv" row-major, "knv" position-major) with `pad` extra elements per
+    innermost row.  Returns (draft, score, status)."""
+    N, K, vocab = logits.shape
+    if dtype == "bf16":
+        base = np.ascontiguousarray(logits).view(np.int16)
+    else:
+        base = np.ascontiguousarray(logits, dtype=np.float32)
+    if layout == "knv":
+        base = np.ascontiguousarray(base.transpose(1, 0, 2))
+    if pad:
+        shp = base.shape[:-1] + (base.shape[-1] + pad,)
+        padded = np.zeros(shp, dtype=base.dtype)
+        padded[..., :vocab] = base
+        base = padded
+    t = up(base)
+    if dtype == "bf16":
+        t = t.view(torch.bfloat16)
+    row = vocab + pad
+    if layout == "knv":
+        stride_n, stride_k = row, N * row
+    else:
+        stride_n, stride_k = K * row, row
+    draft = torch.full((N, K), -1, dtype=torch.int32, device=DEV)
+    score = torch.zeros(N, K, dtype=torch.float32, device=DEV) if with_score else None
+    ws = D.new_workspace(D.dspark_chain_workspace_size(N, K), DEV)
+    D.dspark_chain_draft(t, up_bf16(U), up_bf16(V), up(last.astype(np.int32)),
+                         draft, score, ws, N=N, K=K, vocab=vocab,
+                         rank=U.shape[1], stride_n=stride_n, stride_k=stride_k,
+                         logits_dtype=D.BF16 if dtype == "bf16" else D.F32)
+    torch.cuda.synchronize()
+    st = D.dspark_read_status(ws)
+    return (draft.cpu().numpy().astype(np.int64),
+            None if score is None else score.cpu().numpy(), st)
+
+
+def check_chain(got, got_score, logits, dtype, U, V, last, rows=None):
+    """Compares device tokens of `rows` (indices into logits' first axis)
+    with the oracle; returns the number of accepted near-tie divergences."""
+    rows = np.arange(logits.shape[0]) if rows is None else np.asarray(rows)
+    sub = logits[rows]
+    ref = oracle.chain(sub, dtype, U, V, np.asarray(last)[rows])
+    g = got[rows]
+    near = 0
+    U64, V64 = oracle.bf16_to_f64(U), oracle.bf16_to_f64(V)
+    for i in range(len(rows)):
+        diverged = False
+        prev_tok = None
+        for k in range(sub.shape[1]):
+            if not diverged:
+                if g[i, k] == ref["draft"][i, k]:
+                    if got_score is not None:
+                        _score_ok(got_score[rows[i], k], ref["score"][i, k])
+                    continue
+                # tolerated only at a near-tie of the oracle's own values
+                mx, mg = ref["score"][i, k], ref["margin"][i, k]
+                tol = NEAR_TIE * abs(mx)
+                r = oracle.chain_position(
+                    oracle.to_f64(sub[i:i + 1, k, :], dtype), U64, V64,
+                    np.array([_prev(ref["draft"], last, rows, i, k)]))
+                assert mg < tol and r["adj"][0, g[i, k]] >= mx - tol, \
+                    (rows[i], k, g[i, k], ref["draft"][i, k], mx, mg)
+                near += 1
+                diverged = True
+                prev_tok = g[i, k]
+                continue
+            # validity of the rest of a diverged row, given the device's
+            # own previous token
+            r = oracle.chain_position(oracle.to_f64(sub[i:i + 1, k, :], dtype),
+                                      U64, V64, np.array([prev_tok]))
+            mx = r["score"][0]
+            tol = NEAR_TIE * abs(mx)
+            assert r["adj"][0, g[i, k]] >= mx - tol, (rows[i], k)
+            if g[i, k] != r["tok"][0]:
+                assert r["margin"][0] < tol
+            prev_tok = g[i, k]
+    return near
+
+
+def _prev(draft, last, rows, i, k):
+    if k == 0:
+        p = int(np.asarray(last)[rows[i]])
+        return p
+    return int(draft[i, k - 1])
+
+
+def _score_ok(got, want):
+    if np.isnan(want):
+        assert np.isnan(got)
+        return
+    assert abs(float(got) - want) <= SCORE_RTOL * max(abs(want), 1e-3), (got, want)
+
+
+# ----------------------------------------------------------- scheduler
+def run_select(conf, mask, cost, T, draft_cost=0.0, flags=0, draft=None,
+               fused=True):
+    """Runs the scheduler through the fused call or the four separate calls;
+    returns numpy outputs and the status word."""
+    N, K = conf.shape
+    d_conf = up(np.asarray(conf, np.float32))
+    d_mask = None if mask is None else up(np.asarray(mask, np.uint8))
+    d_cost = up(np.asarray(cost, np.float32))
+    d_T = up(np.array([T], np.int32))
+    d_draft = None if draft is None else up(np.asarray(draft, np.int32))
+    surv = torch.zeros(N, K, dtype=torch.float32, device=DEV)
+    srt = torch.full((N * K,), -1, dtype=torch.int32, device=DEV)
+    pre = torch.full((N * K + 1,), -1.0, dtype=torch.float64, device=DEV)
+    ne, ns, B = i32(1), i32(1), i32(1)
+    obj = torch.zeros(1, dtype=torch.float64, device=DEV)
+    ln, cu = i32(N), i32(N + 1)
+    vi = torch.full((N * K,), -1, dtype=torch.int32, device=DEV)
+    vt = torch.full((N * K,), -1, dtype=torch.int32, device=DEV)
+    ws = D.new_workspace(D.dspark_select_workspace_size(N, K, len(cost)), DEV)
+    if fused:
+        D.dspark_select_step(d_conf, d_mask, d_cost, d_T, draft_cost, flags,
+                             d_draft, surv, srt, pre, ne, ns, B, obj, ln, cu,
+                             vi, vt if d_draft is not None else None, ws)
+    else:
+        D.dspark_survival_topb(d_conf, d_mask, surv, srt, pre, ne, ns, ws)
+        D.dspark_choose_budget(pre, ne, ns, d_cost, d_T, draft_cost, flags, B,
+                               obj, ws)
+        D.dspark_allocate_prefix(srt, B, N, K, ln, ws)
+        D.dspark_compact_verify(ln, d_draft, N, K, cu, vi,
+                                vt if d_draft is not None else None, ws)
+    torch.cuda.synchronize()
+    st = D.dspark_read_status(ws)
+    out = dict(survival=surv.cpu().numpy(), sorted=srt.cpu().numpy(),
+               prefix=pre.cpu().numpy(), n_eligible=int(ne.item()),
+               n_sampling=int(ns.item()), B=int(B.item()),
+               objective=float(obj.item()), draft_len=ln.cpu().numpy(),
+               cu_len=cu.cpu().numpy(), verify_idx=vi.cpu().numpy(),
+               verify_tok=vt.cpu().numpy(), status=st)
+    return out
+
+
+def check_select(got, conf, mask, cost, T, draft_cost=0.0, flags=0, draft=None):
+    N, K = np.asarray(conf).shape
+    r = oracle.select_step(conf, mask, cost, T, draft_cost, flags, draft)
+    S = r["n_eligible"]
+    # survival: fp64 product rounded once to fp32 on both sides
+    np.testing.assert_array_equal(got["survival"], r["survival"].astype(np.float32))
+    assert got["n_eligible"] == S and got["n_sampling"] == r["n_sampling"]
+    np.testing.assert_array_equal(got["sorted"][:S], r["order"])
+    # exact prefix sums: identical bits
+    np.testing.assert_array_equal(got["prefix"][:S + 1], r["prefix"])
+    assert got["B"] == r["B"], (got["B"], r["B"])
+    if np.isnan(r["objective"]):
+        assert np.isnan(got["objective"])
+    else:
+        assert got["objective"] == r["objective"], (got["objective"], r["objective"])
+    np.testing.assert_array_equal(got["draft_len"], r["draft_len"])
+    np.testing.assert_array_equal(got["cu_len"], r["cu_len"])
+    B = r["B"]
+    np.testing.assert_array_equal(got["verify_idx"][:B], r["verify_idx"])
+    assert np.all(got["verify_idx"][B:] == -1)
+    if draft is not None:
+        np.testing.assert_array_equal(got["verify_tok"][:B], r["verify_tok"])
+    want_status = r["status"]
+    assert got["status"] == want_status, (got["status"], want_status)
+    return r

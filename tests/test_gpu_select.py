@@ -1,0 +1,137 @@
+"""GPU parity of the scheduler calls against the oracle, bit for bit.
+
+"Adaptive Verification in vLLM", *Scheduling the budget* and *The cost
+model*.  Every output (survival, order, exact prefix sums, B, objective,
+lengths, offsets, verify list, status bits) must equal the oracle's.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _both(conf, mask, cost, T, draft_cost=0.0, flags=0, draft=None):
+    from gpu_harness import run_select, check_select
+    for fused in (True, False):
+        got = run_select(conf, mask, cost, T, draft_cost, flags, draft, fused=fused)
+        r = check_select(got, conf, mask, cost, T, draft_cost, flags, draft)
+    return r
+
+
+def test_w1_fig1():
+    d = workloads.w1_instance()
+    r = _both(d["conf"], d["mask"], d["cost"], d["T"])
+    assert r["B"] == 11
+
+
+def test_w2_cost_index():
+    with open(os.path.join(GOLD, "w2_cost_index.json")) as f:
+        g = json.load(f)
+    r = _both(np.array(g["conf"], np.float32), np.array(g["mask"], np.uint8),
+              np.array(g["cost"], np.float32), g["T"])
+    assert r["B"] == g["expected"]["B"]
+
+
+@pytest.mark.parametrize("name", list(workloads.CONFIGS))
+def test_workload(name):
+    cfg = workloads.get_config(name)
+    d = workloads.make_select_inputs(cfg)
+    flags = oracle.FORCE_RUNNING_MAX if cfg.cost_kind == "noisy" else 0
+    rng = np.random.default_rng(cfg.seed)
+    draft = rng.integers(0, cfg.vocab, size=(cfg.N, cfg.K)).astype(np.int32)
+    _both(d["conf"], d["mask"], d["cost"], d["T"], 0.0, flags, draft)
+
+
+def test_stress_table_forced_by_prep_call():
+    import torch
+    from gpu_harness import up
+    from speculative_decoding_draft_dspark_gb300 import dspark as D
+    cfg = workloads.get_config("stress")
+    d = workloads.make_select_inputs(cfg)
+    for mode in (D.COST_FORCE_MONOTONE, D.COST_FORCE_SUFFIX_MIN):
+        c = up(d["cost"])
+        out = torch.empty_like(c)
+        D.dspark_force_monotone(c, out, mode)
+        D.dspark_force_monotone(c, c, mode)            # in place
+        torch.cuda.synchronize()
+        want = oracle.force_monotone(d["cost"], mode)
+        np.testing.assert_array_equal(out.cpu().numpy(), want)
+        np.testing.assert_array_equal(c.cpu().numpy(), want)
+    forced = oracle.force_monotone(d["cost"])
+    _both(d["conf"], d["mask"], forced, d["T"])
+
+
+@pytest.mark.parametrize("flags", [0, 1, 2, 4, 5, 6])
+def test_flags_on_staircase(flags):
+    cfg = workloads.get_config("dsv4")
+    d = workloads.make_select_inputs(cfg)
+    cost = d["cost"].copy()
+    rng = np.random.default_rng(77)
+    cost *= rng.uniform(0.97, 1.03, size=cost.shape).astype(np.float32)
+    for T in (0, 100, 2288, 4000, 8000):
+        _both(d["conf"], d["mask"], cost, T, 1.5, flags)
+
+
+def test_edges():
+    rng = np.random.default_rng(5)
+    cost = (10 + 0.5 * np.arange(64)).astype(np.float32)
+    conf = rng.uniform(0, 1, (3, 7)).astype(np.float32)
+    for T in (-5, 0, 62, 63, 64, 1000):             # table edges
+        _both(conf, None, cost, T)
+    _both(conf, np.zeros(3, np.uint8), cost, 3)       # nobody samples
+    _both(conf[:1], None, cost, 3)                   # one request
+    _both(conf[:, :1], None, cost, 3)                # K = 1
+    bad = conf.copy()
+    bad[0, 1] = np.nan
+    bad[1, 2] = 1.5
+    bad[2, 0] = -0.25
+    bad[2, 3] = -0.0
+    _both(bad, None, cost, 3)                         # clamped + flagged
+    ones = conf.copy()
+    ones[:, 2:5] = 1.0                                # survival ties
+    _both(ones, None, cost, 3)
+    zcost = cost.copy()
+    zcost[10] = 0.0
+    zcost[12] = -1.0
+    _both(conf, None, zcost, 3)                       # non-positive cost
+    ncost = cost.copy()
+    ncost[9] = np.nan
+    for fl in (0, 1, 2, 4):
+        _both(conf, None, ncost, 3, 0.0, fl)          # NaN cost
+
+
+@pytest.mark.parametrize("N,K", [(1, 32), (512, 32), (16384, 1), (2048, 8),
+                                 (1000, 15), (37, 3)])
+def test_sizes(N, K):
+    rng = np.random.default_rng(N * 100 + K)
+    conf = rng.uniform(0, 1, (N, K)).astype(np.float32) ** 0.3
+    conf[rng.uniform(size=(N, K)) < 0.02] = 1.0
+    mask = (rng.uniform(size=N) < 0.9).astype(np.uint8)
+    L = N * K + 50
+    base = 100 + 0.01 * np.arange(L)
+    cost = (base * rng.uniform(0.99, 1.01, L)).astype(np.float32)
+    T = int(rng.integers(0, 40))
+    _both(conf, mask, cost, T, 0.0, oracle.FORCE_RUNNING_MAX)
+
+
+def test_tiny_survivals_exact_sums():
+    """Survivals spanning hundreds of binary orders of magnitude."""
+    rng = np.random.default_rng(8)
+    conf = rng.uniform(0, 1, (64, 32)).astype(np.float32) ** 8
+    conf[:4, :] = 1e-30
+    cost = (5 + 0.001 * np.arange(4096)).astype(np.float32)
+    _both(conf, None, cost, 1)
