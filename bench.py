@@ -1,0 +1,526 @@
+#!/usr/bin/env python3
+"""Benchmark of the DSpark draft-and-schedule step on one GB300 per rank.
+
+One step = dspark_chain_draft (K = 7 positions of bias GEMM + fused
+bias-add/argmax) followed by dspark_select_step (survival, global order,
+exact prefix sums, budget, allocation, compaction) over the headline
+workload: batch 256, K 7, vocabulary 262144, rank 256, with the DeepSeek-V4
+confidence, sampling-mask and stepped cost-table recipe (seeded synthetic
+inputs; the pages' datasets are not reproduced).  The two calls are captured
+in CUDA graphs and replayed; the timed region replays exactly --steps steps
+with CUDA events on the launching stream.  The inputs (939.5 MB of logits,
+134 MB of V) are larger than L2, so no flush is needed between steps.
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle instead.
+Multi-GPU (torchrun): every rank runs an independent replica on its own
+batch (the step has no cross-request exchange in the chain; see the design
+notes), the timed region is bracketed by barriers and the maximum time over
+ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("µs per draft-chain+schedule step at batch 256, K=7, vocab "
+          "262144; % of roofline")
+WORKLOAD = "headline"
+CHAIN_SRC = os.path.join(ROOT, "speculative_decoding_draft_dspark_gb300",
+                         "csrc", "chain.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "chain_position_headline_ncu.md")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch eagerly instead of replaying CUDA graphs")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def algorithmic_bytes_per_launch(cfg) -> float:
+    """Minimum HBM bytes of one chain launch (one draft position): the
+    position's logits slice, V read once per step (amortised over the K
+    launches), the gathered U rows and the token reads/writes."""
+    esz = 2 if cfg.logits_dtype == "bf16" else 4
+    logits = cfg.N * cfg.vocab * esz
+    v_once = cfg.vocab * cfg.rank * 2 / cfg.K
+    u_rows = cfg.N * cfg.rank * 2
+    tokens = cfg.N * 4 * 2
+    return logits + v_once + u_rows + tokens
+
+
+def flops_per_launch(cfg) -> float:
+    return 2.0 * cfg.N * cfg.vocab * cfg.rank
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), \
+            d.get("bf16_tflops_sustained", 1700.0), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current chain kernel source (else None)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    src_hash = hashlib.sha256(open(CHAIN_SRC, "rb").read()).hexdigest()[:16]
+    bytes_ = None
+    hash_ok = False
+    for line in open(TRAFFIC_FILE):
+        if line.startswith("kernel_source_sha256_16:"):
+            hash_ok = line.split(":", 1)[1].strip() == src_hash
+        if line.startswith("dram_bytes_per_launch:"):
+            bytes_ = float(line.split(":", 1)[1].strip())
+    return bytes_ if hash_ok else None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = os.path.join("/tmp", f"dspark_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.out, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.out):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                 active=parts[4], hw=parts[5], hwt=parts[6],
+                                 swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.out)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            if r["hw"] == "Active":
+                reasons.add("hw_slowdown")
+            if r["hwt"] == "Active":
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"] == "Active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"] == "Active":
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["smax"] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------- GPU arm
+class Step:
+    """Device-resident inputs and outputs of one headline step, and the two
+    calls that make the step."""
+
+    def __init__(self, cfg, device, seed_offset=0):
+        import numpy as np
+        import torch
+        import workloads
+        from speculative_decoding_draft_dspark_gb300 import dspark as D
+        self.D = D
+        self.cfg = cfg
+        dev = device
+        self.sel = workloads.make_select_inputs(cfg)
+        self.fac = workloads.make_chain_factors(cfg)
+        self.last_np = workloads.make_last_token(cfg)
+        self.logits_np = workloads.make_logits_rows(cfg)
+        up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+        bf = lambda a: up(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+        self.logits = bf(self.logits_np) if cfg.logits_dtype == "bf16" else up(self.logits_np)
+        self.U, self.V = bf(self.fac["U"]), bf(self.fac["V"])
+        self.last = up(self.last_np)
+        self.conf, self.mask = up(self.sel["conf"]), up(self.sel["mask"])
+        self.cost = up(self.sel["cost"])
+        self.T = torch.tensor([self.sel["T"]], dtype=torch.int32, device=dev)
+        N, K = cfg.N, cfg.K
+        i32 = lambda n: torch.zeros(n, dtype=torch.int32, device=dev)  # noqa: E731
+        self.draft = torch.zeros(N, K, dtype=torch.int32, device=dev)
+        self.score = torch.zeros(N, K, dtype=torch.float32, device=dev)
+        self.surv = torch.zeros(N, K, dtype=torch.float32, device=dev)
+        self.srt = i32(N * K)
+        self.pre = torch.zeros(N * K + 1, dtype=torch.float64, device=dev)
+        self.ne, self.ns, self.B = i32(1), i32(1), i32(1)
+        self.obj = torch.zeros(1, dtype=torch.float64, device=dev)
+        self.ln, self.cu, self.vi, self.vt = i32(N), i32(N + 1), i32(N * K), i32(N * K)
+        self.cws = D.new_workspace(D.dspark_chain_workspace_size(N, K), dev)
+        self.sws = D.new_workspace(D.dspark_select_workspace_size(N, K, len(self.sel["cost"])), dev)
+        self.flags = D.COST_FORCE_MONOTONE if cfg.cost_kind == "noisy" else 0
+
+    def chain(self):
+        self.D.dspark_chain_draft(self.logits, self.U, self.V, self.last,
+                                  self.draft, self.score, self.cws)
+
+    def select(self):
+        self.D.dspark_select_step(self.conf, self.mask, self.cost, self.T, 0.0,
+                                  self.flags, self.draft, self.surv, self.srt,
+                                  self.pre, self.ne, self.ns, self.B, self.obj,
+                                  self.ln, self.cu, self.vi, self.vt, self.sws)
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import workloads
+    import __graft_entry__
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    __graft_entry__.build()
+    cfg = workloads.get_config(args.workload)
+    st = Step(cfg, dev)
+    D = st.D
+    stream = torch.cuda.Stream(device=dev)
+
+    # eager warm-up (also sets the kernels' shared-memory attributes)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            st.chain()
+            st.select()
+    stream.synchronize()
+    assert D.dspark_read_status(st.cws) == 0 and D.dspark_read_status(st.sws) == 0
+
+    if args.no_graph:
+        run_chain, run_select = st.chain, st.select
+    else:
+        g_chain, g_sel = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_chain, stream=stream):
+            st.chain()
+        with torch.cuda.graph(g_sel, stream=stream):
+            st.select()
+        run_chain, run_select = g_chain.replay, g_sel.replay
+
+    K_steps, W = args.steps, args.warmup
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K_steps)]
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            run_chain()
+            run_select()
+    stream.synchronize()
+
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)  # let the sampler come up
+    t_host0 = time.perf_counter()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(K_steps):
+            ev[i][0].record(stream)
+            run_chain()
+            ev[i][1].record(stream)
+            run_select()
+            ev[i][2].record(stream)
+        end.record(stream)
+    torch.cuda.synchronize()
+    t_host = time.perf_counter() - t_host0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(end)
+    chain_us = [ev[i][0].elapsed_time(ev[i][1]) * 1e3 for i in range(K_steps)]
+    sel_us = [ev[i][1].elapsed_time(ev[i][2]) * 1e3 for i in range(K_steps)]
+    step_us = [ev[i][0].elapsed_time(ev[i][2]) * 1e3 for i in range(K_steps)]
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # outputs of the timed steps are still the oracle's (cheap integrity check)
+    assert D.dspark_read_status(st.cws) == 0 and D.dspark_read_status(st.sws) == 0
+
+    ms_per_iter = total_ms / K_steps
+    value_us = ms_per_iter * 1e3 / world   # job-wide microseconds per step
+    hbm, tf_burst, tf_sus, peak_src = measured_peaks()
+    chain_med = statistics.median(chain_us)
+    per_launch_s = chain_med * 1e-6 / cfg.K
+    achieved_gbs = algorithmic_bytes_per_launch(cfg) / per_launch_s / 1e9
+    achieved_tf = flops_per_launch(cfg) / per_launch_s / 1e12
+    traffic = recorded_traffic()
+    q = lambda xs, p: float(np.percentile(np.array(xs), p))  # noqa: E731
+
+    result = {
+        "metric": METRIC, "value": round(value_us, 3), "unit": "us/step",
+        "n_gpus": world, "steps": K_steps, "warmup": W,
+        "ms_per_step": round(ms_per_iter, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded numpy; shapes and distributions of the "
+                "pages' workloads)",
+        "config": {
+            "workload": f"{cfg.name}: batch {cfg.N}, K {cfg.K}, vocab "
+                        f"{cfg.vocab}, rank {cfg.rank}, bf16 logits/U/V, "
+                        f"{cfg.n_nonsampling} chunked-prefill requests, T={cfg.T}, "
+                        f"cost table L={cfg.L} stepped to 4096",
+            "timing": "CUDA graphs (chain, select) replayed; CUDA events on "
+                      "the launching stream",
+            "l2": "inputs larger than L2 (logits 939.5 MB, V 134.2 MB); no flush",
+            "parallelism": f"replicas x{world}",
+        },
+        "breakdown_us": {
+            "chain_median": round(chain_med, 3), "chain_p10": round(q(chain_us, 10), 3),
+            "chain_p90": round(q(chain_us, 90), 3),
+            "select_median": round(statistics.median(sel_us), 3),
+            "select_p10": round(q(sel_us, 10), 3), "select_p90": round(q(sel_us, 90), 3),
+            "step_median": round(statistics.median(step_us), 3),
+            "host_clock_us_per_step": round(t_host * 1e6 / K_steps, 3),
+        },
+        "roofline": {
+            "bound": "hbm", "kernel": "chain_position_kernel (per launch = one position)",
+            "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved_gbs / hbm, 4), "traffic": traffic,
+            "algorithmic_bytes_per_launch": algorithmic_bytes_per_launch(cfg),
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+        },
+        "roofline_tensor": {
+            "bound": "tensor", "achieved": round(achieved_tf, 2),
+            "peak": tf_burst, "unit": "TFLOP/s",
+            "frac": round(achieved_tf / tf_burst, 4),
+            "frac_of_sustained": round(achieved_tf / tf_sus, 4),
+            "flops_per_launch": flops_per_launch(cfg),
+        },
+        "gpu_launches": K_steps * (cfg.K + 1),
+        "clocks": clocks,
+    }
+    if rank == 0:
+        result["e2e"] = run_e2e(st, cfg, stream, args.e2e_steps)
+        if world == 1 and not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(cfg)
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(st, cfg, stream, steps):
+    """The same step through the public API with host buffers: per step the
+    inputs are copied from pinned host memory and the scheduler's results
+    are read back, all inside the timed region."""
+    import numpy as np
+    import torch
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_logits = pin(st.logits_np.view(np.int16) if cfg.logits_dtype == "bf16" else st.logits_np)
+    h_conf, h_mask = pin(st.sel["conf"]), pin(st.sel["mask"])
+    h_last = pin(st.last_np)
+    h_T = torch.tensor([st.sel["T"]], dtype=torch.int32).pin_memory()
+    outs = [st.B, st.ln, st.cu, st.vi, st.vt, st.draft]
+    h_outs = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    d_logits_raw = st.logits.view(torch.int16) if cfg.logits_dtype == "bf16" else st.logits
+    h2d = sum(t.numel() * t.element_size() for t in (h_logits, h_conf, h_mask, h_last, h_T))
+    d2h = sum(t.numel() * t.element_size() for t in h_outs)
+
+    def one():
+        d_logits_raw.copy_(h_logits, non_blocking=True)
+        st.conf.copy_(h_conf, non_blocking=True)
+        st.mask.copy_(h_mask, non_blocking=True)
+        st.last.copy_(h_last, non_blocking=True)
+        st.T.copy_(h_T, non_blocking=True)
+        st.chain()
+        st.select()
+        for d, h in zip(outs, h_outs):
+            h.copy_(d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one()
+    stream.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        s.record(stream)
+        for _ in range(steps):
+            one()
+        e.record(stream)
+    stream.synchronize()
+    us = s.elapsed_time(e) * 1e3 / steps
+    return {"value": round(us, 2), "unit": "us/step", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "path": "pinned host -> device copies, dspark_chain_draft, "
+                    "dspark_select_step, device -> pinned host copies"}
+
+
+# ------------------------------------------------------- CPU oracle leg
+def _oracle_data(cfg):
+    import workloads
+    sel = workloads.make_select_inputs(cfg)
+    fac = workloads.make_chain_factors(cfg)
+    return dict(logits=workloads.make_logits_rows(cfg), U=fac["U"], V=fac["V"],
+                last=workloads.make_last_token(cfg), conf=sel["conf"],
+                mask=sel["mask"], cost=sel["cost"], T=sel["T"])
+
+
+def _flags(cfg):
+    import oracle
+    return oracle.FORCE_RUNNING_MAX if cfg.cost_kind == "noisy" else 0
+
+
+def cpu_baseline(cfg):
+    """The oracle as it stands, on this host's cores, over one full step
+    (all requests, all positions, then the scheduler)."""
+    import oracle
+    data = _oracle_data(cfg)
+    t0 = time.perf_counter()
+    ch = oracle.chain(data["logits"], cfg.logits_dtype, data["U"], data["V"],
+                      data["last"])
+    t1 = time.perf_counter()
+    oracle.select_step(data["conf"], data["mask"], data["cost"], data["T"], 0.0,
+                       _flags(cfg), ch["draft"])
+    t2 = time.perf_counter()
+    return {"value": round((t2 - t0) * 1e6, 1), "unit": "us/step",
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"one full step of the {cfg.name} workload (all {cfg.N} "
+                      f"requests x {cfg.K} positions, then the scheduler): "
+                      f"chain {t1 - t0:.2f} s, scheduler {t2 - t1:.3f} s; "
+                      f"numpy fp64, BLAS on all cores"}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle, timed as it stands on this host.
+
+    The fp64 copies of the Markov factors are made once (they are constant
+    weights).  Each timed step runs the whole scheduler and one chain
+    position (cycling k) for a sample of requests; the step estimate is
+    scheduler + K x (position time at the sample + the remaining requests x
+    the per-request slope measured in warm-up).  The sample size is chosen
+    so that the whole run stays within a few minutes."""
+    import numpy as np
+    import oracle
+    import workloads
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    cfg = workloads.get_config(args.workload)
+    data = _oracle_data(cfg)
+    U64, V64 = oracle.bf16_to_f64(data["U"]), oracle.bf16_to_f64(data["V"])
+    draft = np.zeros((cfg.N, cfg.K), np.int64)
+
+    def position(rows, k):
+        prev = data["last"][rows] if k == 0 else draft[rows, k - 1]
+        t0 = time.perf_counter()
+        r = oracle.chain_position(oracle.to_f64(data["logits"][rows, k, :],
+                                                cfg.logits_dtype), U64, V64, prev)
+        dt = time.perf_counter() - t0
+        draft[rows, k] = r["tok"]
+        return dt
+
+    def select():
+        t0 = time.perf_counter()
+        oracle.select_step(data["conf"], data["mask"], data["cost"], data["T"],
+                           0.0, _flags(cfg), draft)
+        return time.perf_counter() - t0
+
+    rng = np.random.default_rng(0)
+    # warm-up and calibration of the per-request slope
+    small, large = 4, min(cfg.N, 64)
+    t_small = min(position(np.arange(small), 0) for _ in range(2))
+    t_large = min(position(np.arange(large), 0) for _ in range(2))
+    slope = max(0.0, (t_large - t_small) / (large - small))
+    t_sel = select()
+    budget_s = 150.0
+    per_step = budget_s / max(1, args.steps + args.warmup)
+    r = int(max(1, min(cfg.N, small + (per_step - t_sel - t_small) / max(slope, 1e-9))))
+    samples = []
+    for i in range(args.warmup + args.steps):
+        k = i % cfg.K
+        rows = np.sort(rng.choice(cfg.N, r, replace=False))
+        tp = position(rows, k)
+        ts = select()
+        if i >= args.warmup:
+            samples.append(ts + cfg.K * (tp + (cfg.N - r) * slope))
+    us = statistics.mean(samples) * 1e6
+    sample_txt = (f"per step: the whole scheduler plus one chain position for "
+                  f"{r} of {cfg.N} requests; estimate = scheduler + {cfg.K} x "
+                  f"(position time + {cfg.N - r} x {slope * 1e3:.3f} ms per "
+                  f"request, slope measured at {small} and {large} requests); "
+                  f"fp64 factors converted once")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1),
+        "unit": "us/step", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded numpy)",
+        "config": {"workload": f"{cfg.name}: batch {cfg.N}, K {cfg.K}, vocab "
+                               f"{cfg.vocab}, rank {cfg.rank}"},
+        "cpu_baseline": {"value": round(us, 1), "unit": "us/step",
+                         "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample_txt},
+        "e2e": {"value": round(us, 1), "unit": "us/step",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -6,8 +6,8 @@
 // Inference", section "Draft better": the Markov head is a rank-256
 // factorisation that adjusts each word's odds using only the word before it.
 //
-// One launch per draft position k.  Per launch, for the 128-request tile m
-// and the vocabulary tiles a CTA owns:
+// One persistent, cooperative launch chains all K positions.  For draft
+// position k, the 128-request tile m and the vocabulary tiles a CTA owns:
 //
 //   A = U[prev_m]        128 x r   bf16, gathered into shared memory
 //   B = V[v0 : v0+256]   256 x r   bf16, streamed by TMA
@@ -18,16 +18,20 @@
 // so the [N x vocab] bias never leaves the SM.  The per-CTA winners are
 // combined with one 64-bit atomicMax per row on a key
 // (orderable(value) << 32) | (0xFFFFFFFF - index): larger value wins, then
-// smaller index; NaN maps to the largest key.  The last CTA to finish writes
-// draft[:, k] (and the score), which the next position's launch gathers from
-// after a programmatic-dependent-launch wait.
+// smaller index; NaN maps to the largest key.  Position k+1 needs every
+// row's winner of position k, so the epilogue warps meet at a grid barrier
+// (a counter per position, polled with a time limit; the cooperative launch
+// keeps all CTAs resident) and then each warp decodes the winners of its own
+// 32 rows and gathers their U rows.  The TMA producers do not depend on the winners and
+// keep streaming V and logits across position boundaries.
 //
 // Warp roles (256 threads, one CTA per SM, all 512 TMEM columns):
 //   warp 0      TMA producer of V tiles (4 K-blocks of 64 per tile)
 //   warp 1      TMEM allocation; one thread issues tcgen05.mma
 //   warp 2      TMA producer of logits boxes
 //   warp 3      idle
-//   warps 4-7   gather of U rows, then the epilogue (TMEM lane quarter w%4)
+//   warps 4-7   grid barrier, winner decode and U gather, then the epilogue
+//               (TMEM lane quarter w % 4)
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
@@ -38,7 +42,9 @@
 namespace dspark {
 
 constexpr int BM = 128;  // requests per tile (MMA M)
-constexpr int BN = 256;  // vocabulary entries per tile (MMA N)
+constexpr int BN = 256;  // vocabulary entries per tile (MMA N, at most)
+constexpr int BQ = 64;   // vocabulary quantum: tiles are 1..4 quanta wide
+constexpr int QPT = BN / BQ;  // quanta per full tile
 constexpr int BK = 64;   // rank entries per K-block (128 bytes of bf16)
 constexpr int MAX_KB = 4;
 constexpr int NUM_B_STAGES = 3;
@@ -46,6 +52,7 @@ constexpr int NUM_L_STAGES = 4;
 constexpr int A_KBLOCK_BYTES = BM * 128;
 constexpr int A_BYTES = MAX_KB * A_KBLOCK_BYTES;
 constexpr int B_STAGE_BYTES = BN * 128;
+constexpr int B_BOX_BYTES = BQ * 128;  // one quantum of one K-block
 constexpr int L_STAGE_BYTES = BM * 128;
 constexpr int SMEM_A_OFF = 0;
 constexpr int SMEM_B_OFF = SMEM_A_OFF + A_BYTES;
@@ -56,7 +63,9 @@ constexpr int SMEM_USED = SMEM_BAR_OFF + NUM_BARS * 8 + 16;
 constexpr int CHAIN_SMEM_BYTES = SMEM_USED + 1024;  // 1 KB alignment slack
 constexpr int CHAIN_THREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;  // two 256-column fp32 accumulators
-constexpr uint32_t IDESC = umma_idesc_bf16_f32(BM, BN);
+// bytes of V worth protecting in L2 across positions (measured on GB300:
+// protecting more than this lets the logits stream evict it anyway)
+constexpr double kL2KeepBytes = 40.0 * 1024 * 1024;
 
 static_assert(CHAIN_SMEM_BYTES <= 232448, "shared memory budget");
 
@@ -65,18 +74,36 @@ struct ChainParams {
   const int32_t *last_token;
   int32_t *draft;
   float *score;
-  unsigned long long *slots;  // [N] winners of this position
-  uint32_t *counter;          // CTAs finished with this position
+  unsigned long long *slots;  // [K][N] per-row winners
+  uint32_t *counters;         // [K][n_mtiles] epilogue warps done
+  uint32_t *g_abort;          // set by any CTA that gives up
   uint32_t *status;
-  int32_t N, K, vocab, rank, k_pos;
-  int32_t n_mtiles, n_vgroups, n_vtiles;
+  int32_t N, K, vocab, rank;
+  int32_t n_mtiles, n_vgroups, n_quanta;
   int32_t l_k_is_dim1;  // logits map: dim1 = K, dim2 = N (else swapped)
+  int32_t v_keep_tenths;
 };
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
-                                              volatile uint32_t *abort_flag,
-                                              uint32_t *status) {
-  return wait_bounded(bar, parity, abort_flag, status);
+// Tile i of position k over the quanta [qb, qe) a CTA owns: even positions
+// sweep upwards from qb, odd ones downwards from qe (the V tiles read last
+// for position k are read first for k+1, while still in L2).  Every tile is
+// QPT quanta wide except the last one processed.
+struct TileGeom {
+  int qa;  // first quantum
+  int nq;  // quanta in the tile (1..QPT)
+};
+
+__device__ __forceinline__ TileGeom tile_geom(int k, int i, int qb, int qe) {
+  TileGeom g;
+  if ((k & 1) == 0) {
+    g.qa = qb + QPT * i;
+    g.nq = min(QPT, qe - g.qa);
+  } else {
+    const int top = qe - QPT * i;
+    g.qa = max(qb, top - QPT);
+    g.nq = top - g.qa;
+  }
+  return g;
 }
 
 // bounded wait that ignores the abort flag (teardown of copies in flight)
@@ -92,13 +119,51 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity,
   }
 }
 
+// An epilogue warp waits until every epilogue warp of the CTAs sharing its
+// 128-request tile has published position k (4 arrivals per CTA; the tiles
+// are independent chains).  Lane 0 polls with a time limit; the warp leaves
+// together.  No barrier spans warps, so a warp that gives up can never leave
+// another one blocked.
+__device__ __forceinline__ bool grid_wait(const ChainParams &p, int k,
+                                          int m_tile,
+                                          volatile uint32_t *cta_abort) {
+  uint32_t r = 1;
+  if ((threadIdx.x & 31) == 0) {
+    const uint32_t target = 4u * static_cast<uint32_t>(p.n_vgroups);
+    const uint32_t *cnt = &p.counters[k * p.n_mtiles + m_tile];
+    if (ld_acquire_gpu(cnt) < target) {
+      const uint64_t t0 = global_timer_ns();
+      while (ld_acquire_gpu(cnt) < target) {
+        if (*cta_abort || *reinterpret_cast<volatile uint32_t *>(p.g_abort)) {
+          r = 0;
+          break;
+        }
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          raise_status(p.status, DSPARK_DEV_TIMEOUT);
+          r = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+  }
+  r = __shfl_sync(0xFFFFFFFFu, r, 0);
+  return r != 0u;
+}
+
+__device__ __forceinline__ int decode_index(unsigned long long key, int vocab) {
+  int idx = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+  if (key == 0ull || idx < 0 || idx >= vocab) idx = 0;
+  return idx;
+}
+
 template <int LDT>
 __global__ void __launch_bounds__(CHAIN_THREADS, 1)
-    chain_position_kernel(const __grid_constant__ CUtensorMap tmV,
-                          const __grid_constant__ CUtensorMap tmL,
-                          const ChainParams p) {
+    chain_kernel(const __grid_constant__ CUtensorMap tmV,
+                 const __grid_constant__ CUtensorMap tmL,
+                 const ChainParams p) {
   constexpr int LBOX_COLS = (LDT == DSPARK_BF16) ? 64 : 32;  // 128-byte rows
-  constexpr int NBOX = BN / LBOX_COLS;
+  constexpr int BPQ = BQ / LBOX_COLS;                        // boxes per quantum
   constexpr int CHUNKS_PER_BOX = LBOX_COLS / 32;
 
   extern __shared__ uint8_t smem_raw[];
@@ -116,26 +181,20 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
   uint64_t *mma_done = bars + 19;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NUM_BARS);
   volatile uint32_t *abort_flag = tmem_slot + 1;
-  volatile uint32_t *last_flag = tmem_slot + 2;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int m_tile = blockIdx.x % p.n_mtiles;
   const int grp = blockIdx.x / p.n_mtiles;
   const int m0 = m_tile * BM;
-  const int t_begin =
-      static_cast<int>((static_cast<long long>(grp) * p.n_vtiles) / p.n_vgroups);
-  const int t_end = static_cast<int>(
-      (static_cast<long long>(grp + 1) * p.n_vtiles) / p.n_vgroups);
-  const int nt = t_end - t_begin;
-  // alternate the sweep direction between positions: the V tiles touched
-  // last by position k are the first ones position k+1 reads, while they
-  // are still in L2
-  const bool ascending = (p.k_pos & 1) == 0;
+  const int qb = static_cast<int>((static_cast<long long>(grp) * p.n_quanta) /
+                                  p.n_vgroups);
+  const int qe = static_cast<int>(
+      (static_cast<long long>(grp + 1) * p.n_quanta) / p.n_vgroups);
+  const int nt = (qe - qb + QPT - 1) / QPT;  // tiles per position
   const int KB = (p.rank + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
-    pdl_launch_dependents();
     for (int i = 0; i < NUM_B_STAGES; ++i) {
       mbar_init(&b_full[i], 1);
       mbar_init(&b_empty[i], 1);
@@ -151,7 +210,6 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     mbar_init(a_full, 4);
     mbar_init(mma_done, 1);
     *abort_flag = 0u;
-    *last_flag = 0u;
     fence_mbarrier_init();
     fence_proxy_async_smem();
   }
@@ -171,22 +229,25 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------ V tile producer
     if (lane == 0) {
-      const uint64_t pol = policy_evict_last();
+      const uint64_t pol = policy_keep_tenths(p.v_keep_tenths);
       int last_it[NUM_B_STAGES];
       for (int s = 0; s < NUM_B_STAGES; ++s) last_it[s] = -1;
       int it = 0;
       bool ok = true;
-      for (int i = 0; i < nt && ok; ++i) {
-        const int t = ascending ? t_begin + i : t_end - 1 - i;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int s = it % NUM_B_STAGES;
-          const uint32_t ph = (it / NUM_B_STAGES) & 1;
-          if (!(ok = wait_or_abort(&b_empty[s], ph ^ 1u, abort_flag, p.status)))
-            break;
-          mbar_arrive_expect_tx(&b_full[s], B_STAGE_BYTES);
-          tma_load_2d(smem + SMEM_B_OFF + s * B_STAGE_BYTES, &tmV, &b_full[s],
-                      kb * BK, t * BN, pol);
-          last_it[s] = it;
+      for (int k = 0; k < p.K && ok; ++k) {
+        for (int i = 0; i < nt && ok; ++i) {
+          const TileGeom g = tile_geom(k, i, qb, qe);
+          for (int kb = 0; kb < KB; ++kb, ++it) {
+            const int s = it % NUM_B_STAGES;
+            const uint32_t ph = (it / NUM_B_STAGES) & 1;
+            if (!(ok = wait_bounded(&b_empty[s], ph ^ 1u, abort_flag, p.status)))
+              break;
+            mbar_arrive_expect_tx(&b_full[s], g.nq * B_BOX_BYTES);
+            for (int j = 0; j < g.nq; ++j)
+              tma_load_2d(smem + SMEM_B_OFF + s * B_STAGE_BYTES + j * B_BOX_BYTES,
+                          &tmV, &b_full[s], kb * BK, (g.qa + j) * BQ, pol);
+            last_it[s] = it;
+          }
         }
       }
       if (!ok) {
@@ -201,33 +262,40 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     if (lane == 0) {
       const uint32_t a_base = smem_u32(smem + SMEM_A_OFF);
       const uint32_t b_base = smem_u32(smem + SMEM_B_OFF);
-      bool ok = wait_or_abort(a_full, 0, abort_flag, p.status);
-      if (ok) tc_fence_after();
-      int it = 0;
-      for (int i = 0; i < nt && ok; ++i) {
-        const int buf = i & 1;
-        const uint32_t aph = (i >> 1) & 1;
-        if (!(ok = wait_or_abort(&acc_empty[buf], aph ^ 1u, abort_flag, p.status)))
-          break;
+      int it = 0, ig = 0;
+      bool ok = true;
+      for (int k = 0; k < p.K && ok; ++k) {
+        // A holds this position's gathered U rows
+        if (!(ok = wait_bounded(a_full, k & 1, abort_flag, p.status))) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-        for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int s = it % NUM_B_STAGES;
-          const uint32_t ph = (it / NUM_B_STAGES) & 1;
-          if (!(ok = wait_or_abort(&b_full[s], ph, abort_flag, p.status))) break;
+        for (int i = 0; i < nt && ok; ++i, ++ig) {
+          const TileGeom g = tile_geom(k, i, qb, qe);
+          const uint32_t idesc =
+              umma_idesc_bf16_f32(BM, static_cast<uint32_t>(g.nq * BQ));
+          const int buf = ig & 1;
+          const uint32_t aph = (ig >> 1) & 1;
+          if (!(ok = wait_bounded(&acc_empty[buf], aph ^ 1u, abort_flag, p.status)))
+            break;
           tc_fence_after();
-          const int nk = min(BK, p.rank - kb * BK) / 16;
-          for (int kk = 0; kk < nk; ++kk) {
-            const uint64_t ad =
-                sw128_kmajor_desc(a_base + kb * A_KBLOCK_BYTES + kk * 32);
-            const uint64_t bd =
-                sw128_kmajor_desc(b_base + s * B_STAGE_BYTES + kk * 32);
-            umma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+          for (int kb = 0; kb < KB; ++kb, ++it) {
+            const int s = it % NUM_B_STAGES;
+            const uint32_t ph = (it / NUM_B_STAGES) & 1;
+            if (!(ok = wait_bounded(&b_full[s], ph, abort_flag, p.status))) break;
+            tc_fence_after();
+            const int nk = min(BK, p.rank - kb * BK) / 16;
+            for (int kk = 0; kk < nk; ++kk) {
+              const uint64_t ad =
+                  sw128_kmajor_desc(a_base + kb * A_KBLOCK_BYTES + kk * 32);
+              const uint64_t bd =
+                  sw128_kmajor_desc(b_base + s * B_STAGE_BYTES + kk * 32);
+              umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            umma_commit(&b_empty[s]);  // stage free once these MMAs retire
           }
-          umma_commit(&b_empty[s]);  // stage free once these MMAs retire
+          if (!ok) break;
+          umma_commit(&acc_full[buf]);  // accumulator ready for the epilogue
         }
-        if (!ok) break;
-        umma_commit(&acc_full[buf]);  // accumulator ready for the epilogue
       }
       // every MMA has retired before the CTA frees tensor memory
       umma_commit(mma_done);
@@ -240,21 +308,23 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
       const uint64_t pol = policy_evict_first();
       int last_it[NUM_L_STAGES];
       for (int s = 0; s < NUM_L_STAGES; ++s) last_it[s] = -1;
-      const int c1 = p.l_k_is_dim1 ? p.k_pos : m0;
-      const int c2 = p.l_k_is_dim1 ? m0 : p.k_pos;
       int it = 0;
       bool ok = true;
-      for (int i = 0; i < nt && ok; ++i) {
-        const int t = ascending ? t_begin + i : t_end - 1 - i;
-        for (int j = 0; j < NBOX; ++j, ++it) {
-          const int s = it % NUM_L_STAGES;
-          const uint32_t ph = (it / NUM_L_STAGES) & 1;
-          if (!(ok = wait_or_abort(&l_empty[s], ph ^ 1u, abort_flag, p.status)))
-            break;
-          mbar_arrive_expect_tx(&l_full[s], L_STAGE_BYTES);
-          tma_load_3d(smem + SMEM_L_OFF + s * L_STAGE_BYTES, &tmL, &l_full[s],
-                      t * BN + j * LBOX_COLS, c1, c2, pol);
-          last_it[s] = it;
+      for (int k = 0; k < p.K && ok; ++k) {
+        for (int i = 0; i < nt && ok; ++i) {
+          const TileGeom g = tile_geom(k, i, qb, qe);
+          const int c1 = p.l_k_is_dim1 ? k : m0;
+          const int c2 = p.l_k_is_dim1 ? m0 : k;
+          for (int j = 0; j < g.nq * BPQ; ++j, ++it) {
+            const int s = it % NUM_L_STAGES;
+            const uint32_t ph = (it / NUM_L_STAGES) & 1;
+            if (!(ok = wait_bounded(&l_empty[s], ph ^ 1u, abort_flag, p.status)))
+              break;
+            mbar_arrive_expect_tx(&l_full[s], L_STAGE_BYTES);
+            tma_load_3d(smem + SMEM_L_OFF + s * L_STAGE_BYTES, &tmL, &l_full[s],
+                        g.qa * BQ + j * LBOX_COLS, c1, c2, pol);
+            last_it[s] = it;
+          }
         }
       }
       if (!ok) {
@@ -265,140 +335,177 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ------------------------------------------------ gather + epilogue
+    // ----------------------------- grid barrier, gather, epilogue per k
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     const int m = m0 + row;
     const bool row_ok = m < p.N;
-    // the previous position's tokens are final once its grid has completed
-    pdl_wait_primary();
-    int prev = 0;
-    if (row_ok) {
-      if (p.k_pos == 0) {
-        prev = p.last_token[m];
-        if (prev < 0 || prev >= p.vocab) {
-          prev = 0;
-          raise_status(p.status, DSPARK_DEV_TOKEN_OOR);
+    const bool writer = (grp == 0) && row_ok;  // one CTA per tile writes draft
+    const uint32_t a_base = smem_u32(smem + SMEM_A_OFF);
+    int ig = 0, lit = 0;
+    bool ok = true;
+    for (int k = 0; k < p.K && ok; ++k) {
+      int prev = 0;
+      if (k == 0) {
+        if (row_ok) {
+          prev = p.last_token[m];
+          if (prev < 0 || prev >= p.vocab) {
+            prev = 0;
+            raise_status(p.status, DSPARK_DEV_TOKEN_OOR);
+          }
         }
       } else {
-        prev = p.draft[static_cast<size_t>(m) * p.K + (p.k_pos - 1)];
-      }
-    }
-    const uint16_t *urow = p.U + static_cast<size_t>(prev) * p.rank;
-    const uint32_t a_base = smem_u32(smem + SMEM_A_OFF);
-    for (int kb = 0; kb < KB; ++kb) {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t dst = a_base + kb * A_KBLOCK_BYTES + row * 128 +
-                             ((c ^ (row & 7)) << 4);
-        const int col = kb * BK + c * 8;
-        if (row_ok && col < p.rank)
-          cp_async_16(dst, urow + col);
-        else
-          st_shared_zero16(dst);
-      }
-    }
-    cp_async_commit();
-    cp_async_wait_all();
-    fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
-    __syncwarp();
-    if (lane == 0) mbar_arrive(a_full);
-
-    uint32_t best_key = 0u;  // below every real key
-    int best_idx = 0x7FFFFFFF;
-    int lit = 0;
-    bool ok = true;
-    for (int i = 0; i < nt && ok; ++i) {
-      const int t = ascending ? t_begin + i : t_end - 1 - i;
-      const int buf = i & 1;
-      const uint32_t aph = (i >> 1) & 1;
-      ok = __all_sync(0xFFFFFFFFu,
-                      wait_or_abort(&acc_full[buf], aph, abort_flag, p.status));
-      if (!ok) break;
-      tc_fence_after();
-      const int v_tile0 = t * BN;
-      for (int j = 0; j < NBOX; ++j, ++lit) {
-        const int s = lit % NUM_L_STAGES;
-        const uint32_t lph = (lit / NUM_L_STAGES) & 1;
-        ok = __all_sync(0xFFFFFFFFu,
-                        wait_or_abort(&l_full[s], lph, abort_flag, p.status));
-        if (!ok) break;
-        const uint32_t box =
-            smem_u32(smem + SMEM_L_OFF + s * L_STAGE_BYTES) + row * 128;
-#pragma unroll
-        for (int c = 0; c < CHUNKS_PER_BOX; ++c) {
-          const int col0 = j * LBOX_COLS + c * 32;
-          uint32_t acc[32];
-          tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                 static_cast<uint32_t>(buf * BN + col0),
-                             acc);
-          tmem_ld_wait(acc);
-          float v[32];
-          if constexpr (LDT == DSPARK_BF16) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int chunk = c * 4 + u;
-              const uint4 w = ld_shared_v4(box + ((chunk ^ (row & 7)) << 4));
-              const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                v[u * 8 + 2 * h] =
-                    __uint_as_float(acc[u * 8 + 2 * h]) +
-                    __uint_as_float(ww[h] << 16);
-                v[u * 8 + 2 * h + 1] =
-                    __uint_as_float(acc[u * 8 + 2 * h + 1]) +
-                    __uint_as_float(ww[h] & 0xFFFF0000u);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const uint4 w = ld_shared_v4(box + ((u ^ (row & 7)) << 4));
-              v[u * 4 + 0] = __uint_as_float(acc[u * 4 + 0]) + __uint_as_float(w.x);
-              v[u * 4 + 1] = __uint_as_float(acc[u * 4 + 1]) + __uint_as_float(w.y);
-              v[u * 4 + 2] = __uint_as_float(acc[u * 4 + 2]) + __uint_as_float(w.z);
-              v[u * 4 + 3] = __uint_as_float(acc[u * 4 + 3]) + __uint_as_float(w.w);
-            }
-          }
-          const int vbase = v_tile0 + col0;
-          if (vbase + 32 > p.vocab) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (vbase + e >= p.vocab) v[e] = -INFINITY;
-          }
-          float mx = v[0];
-#pragma unroll
-          for (int e = 1; e < 32; ++e) mx = fmax_nan(mx, v[e]);
-          int ie = 0;
-          if (mx != mx) {
-#pragma unroll
-            for (int e = 31; e >= 0; --e) ie = (v[e] != v[e]) ? e : ie;
-          } else {
-#pragma unroll
-            for (int e = 31; e >= 0; --e) ie = (v[e] == mx) ? e : ie;
-          }
-          const uint32_t key = f32_key(mx);
-          const int idx = vbase + ie;
-          if (key > best_key || (key == best_key && idx < best_idx)) {
-            best_key = key;
-            best_idx = idx;
+        if (!(ok = grid_wait(p, k - 1, m_tile, abort_flag))) break;
+        if (row_ok) {
+          const unsigned long long key = *reinterpret_cast<volatile unsigned long long *>(
+              &p.slots[static_cast<size_t>(k - 1) * p.N + m]);
+          prev = decode_index(key, p.vocab);
+          if (writer) {
+            const uint32_t kh = static_cast<uint32_t>(key >> 32);
+            p.draft[static_cast<size_t>(m) * p.K + (k - 1)] = prev;
+            if (p.score)
+              p.score[static_cast<size_t>(m) * p.K + (k - 1)] = f32_from_key(kh);
+            if (kh == 0xFFFFFFFFu) raise_status(p.status, DSPARK_DEV_NAN_LOGIT);
           }
         }
+      }
+      // gather this position's U rows into A, one 512-byte row per warp
+      // instruction (lane j copies 16-byte chunk j of the row); the MMAs of
+      // position k-1 have all retired, their last accumulator was consumed
+      const int nchunk = KB * 8;
+      for (int r = 0; r < 32; ++r) {
+        const int rp = __shfl_sync(0xFFFFFFFFu, prev, r);
+        const int rrow = q * 32 + r;
+        const bool rok = (m0 + rrow) < p.N;
+        if (lane < nchunk) {
+          const int kb = lane >> 3, c = lane & 7;
+          const uint32_t dst = a_base + kb * A_KBLOCK_BYTES + rrow * 128 +
+                               ((c ^ (rrow & 7)) << 4);
+          if (rok && lane * 8 < p.rank)
+            cp_async_16(dst, p.U + static_cast<size_t>(rp) * p.rank + lane * 8);
+          else
+            st_shared_zero16(dst);
+        }
+      }
+      cp_async_commit();
+      cp_async_wait_all();
+      fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+      __syncwarp();
+      if (lane == 0) mbar_arrive(a_full);
+
+      uint32_t best_key = 0u;  // below every real key
+      int best_idx = 0x7FFFFFFF;
+      for (int i = 0; i < nt && ok; ++i, ++ig) {
+        const TileGeom g = tile_geom(k, i, qb, qe);
+        const int buf = ig & 1;
+        const uint32_t aph = (ig >> 1) & 1;
+        ok = __all_sync(0xFFFFFFFFu,
+                        wait_bounded(&acc_full[buf], aph, abort_flag, p.status));
+        if (!ok) break;
+        tc_fence_after();
+        const int v_tile0 = g.qa * BQ;
+        for (int j = 0; j < g.nq * BPQ; ++j, ++lit) {
+          const int s = lit % NUM_L_STAGES;
+          const uint32_t lph = (lit / NUM_L_STAGES) & 1;
+          ok = __all_sync(0xFFFFFFFFu,
+                          wait_bounded(&l_full[s], lph, abort_flag, p.status));
+          if (!ok) break;
+          const uint32_t box =
+              smem_u32(smem + SMEM_L_OFF + s * L_STAGE_BYTES) + row * 128;
+#pragma unroll
+          for (int c = 0; c < CHUNKS_PER_BOX; ++c) {
+            const int col0 = j * LBOX_COLS + c * 32;
+            uint32_t acc[32];
+            tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(buf * BN + col0),
+                               acc);
+            tmem_ld_wait(acc);
+            float v[32];
+            if constexpr (LDT == DSPARK_BF16) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int chunk = c * 4 + u;
+                const uint4 w = ld_shared_v4(box + ((chunk ^ (row & 7)) << 4));
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                  v[u * 8 + 2 * h] = __uint_as_float(acc[u * 8 + 2 * h]) +
+                                     __uint_as_float(ww[h] << 16);
+                  v[u * 8 + 2 * h + 1] = __uint_as_float(acc[u * 8 + 2 * h + 1]) +
+                                         __uint_as_float(ww[h] & 0xFFFF0000u);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const uint4 w = ld_shared_v4(box + ((u ^ (row & 7)) << 4));
+                v[u * 4 + 0] = __uint_as_float(acc[u * 4 + 0]) + __uint_as_float(w.x);
+                v[u * 4 + 1] = __uint_as_float(acc[u * 4 + 1]) + __uint_as_float(w.y);
+                v[u * 4 + 2] = __uint_as_float(acc[u * 4 + 2]) + __uint_as_float(w.z);
+                v[u * 4 + 3] = __uint_as_float(acc[u * 4 + 3]) + __uint_as_float(w.w);
+              }
+            }
+            const int vbase = v_tile0 + col0;
+            if (vbase + 32 > p.vocab) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (vbase + e >= p.vocab) v[e] = -INFINITY;
+            }
+            float mx = v[0];
+#pragma unroll
+            for (int e = 1; e < 32; ++e) mx = fmax_nan(mx, v[e]);
+            int ie = 0;
+            if (mx != mx) {
+#pragma unroll
+              for (int e = 31; e >= 0; --e) ie = (v[e] != v[e]) ? e : ie;
+            } else {
+#pragma unroll
+              for (int e = 31; e >= 0; --e) ie = (v[e] == mx) ? e : ie;
+            }
+            const uint32_t key = f32_key(mx);
+            const int idx = vbase + ie;
+            if (key > best_key || (key == best_key && idx < best_idx)) {
+              best_key = key;
+              best_idx = idx;
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&l_empty[s]);
+        }
+        if (!ok) break;
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&l_empty[s]);
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
       }
       if (!ok) break;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
-    }
-    if (ok && row_ok) {
-      const unsigned long long packed =
-          (static_cast<unsigned long long>(best_key) << 32) |
-          static_cast<unsigned long long>(0xFFFFFFFFu -
-                                          static_cast<uint32_t>(best_idx));
-      atomicMax(&p.slots[m], packed);
+      // publish this CTA's row winners and arrive at position k's barrier
+      if (row_ok) {
+        const unsigned long long packed =
+            (static_cast<unsigned long long>(best_key) << 32) |
+            static_cast<unsigned long long>(0xFFFFFFFFu -
+                                            static_cast<uint32_t>(best_idx));
+        atomicMax(&p.slots[static_cast<size_t>(k) * p.N + m], packed);
+      }
       __threadfence();
+      __syncwarp();
+      if (lane == 0) atomicAdd(&p.counters[k * p.n_mtiles + m_tile], 1u);
+    }
+    if (ok) {
+      // winners of the last position
+      ok = grid_wait(p, p.K - 1, m_tile, abort_flag);
+      if (ok && writer) {
+        const unsigned long long key = *reinterpret_cast<volatile unsigned long long *>(
+            &p.slots[static_cast<size_t>(p.K - 1) * p.N + m]);
+        const uint32_t kh = static_cast<uint32_t>(key >> 32);
+        p.draft[static_cast<size_t>(m) * p.K + (p.K - 1)] = decode_index(key, p.vocab);
+        if (p.score)
+          p.score[static_cast<size_t>(m) * p.K + (p.K - 1)] = f32_from_key(kh);
+        if (kh == 0xFFFFFFFFu) raise_status(p.status, DSPARK_DEV_NAN_LOGIT);
+      }
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1u;
+      atomicExch(p.g_abort, 1u);
     }
   }
 
@@ -407,28 +514,6 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
-
-  // the last CTA of the grid decodes the winners of every request
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const uint32_t ticket = atomicAdd(p.counter, 1u);
-    *last_flag = (ticket == gridDim.x - 1) ? 1u : 0u;
-  }
-  __syncthreads();
-  if (*last_flag) {
-    __threadfence();
-    for (int n = threadIdx.x; n < p.N; n += blockDim.x) {
-      const unsigned long long key =
-          *reinterpret_cast<volatile unsigned long long *>(&p.slots[n]);
-      const uint32_t kh = static_cast<uint32_t>(key >> 32);
-      int idx = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
-      if (key == 0ull || idx < 0 || idx >= p.vocab) idx = 0;
-      p.draft[static_cast<size_t>(n) * p.K + p.k_pos] = idx;
-      if (p.score)
-        p.score[static_cast<size_t>(n) * p.K + p.k_pos] = f32_from_key(kh);
-      if (kh == 0xFFFFFFFFu) raise_status(p.status, DSPARK_DEV_NAN_LOGIT);
-    }
-  }
 }
 
 // ==========================================================================
@@ -462,14 +547,14 @@ static cudaError_t ensure_kernel_attrs(int dev) {
   std::lock_guard<std::mutex> lk(g_attr_mu);
   if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
   if (!g_attr_done[0][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(chain_position_kernel<DSPARK_BF16>,
+    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DSPARK_BF16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          CHAIN_SMEM_BYTES);
     if (e != cudaSuccess) return e;
     g_attr_done[0][dev] = true;
   }
   if (!g_attr_done[1][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(chain_position_kernel<DSPARK_F32>,
+    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DSPARK_F32>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          CHAIN_SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -478,9 +563,14 @@ static cudaError_t ensure_kernel_attrs(int dev) {
   return cudaSuccess;
 }
 
+static size_t chain_counters_offset(int32_t N, int32_t K) {
+  return kChainSlotsOffset + static_cast<size_t>(N) * K * 8;
+}
+
 size_t chain_workspace_bytes(int32_t N, int32_t K) {
-  const size_t slots = static_cast<size_t>(N) * K * sizeof(unsigned long long);
-  return ((kChainSlotsOffset + slots + 255) / 256) * 256;
+  const size_t n_mtiles = (static_cast<size_t>(N) + BM - 1) / BM;
+  const size_t end = chain_counters_offset(N, K) + n_mtiles * K * 4;
+  return ((end + 255) / 256) * 256;
 }
 
 dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream) {
@@ -494,17 +584,17 @@ dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream) {
   if (n_mtiles > sms) return DSPARK_ERR_UNSUPPORTED;
   if (ensure_kernel_attrs(dev) != cudaSuccess) return DSPARK_ERR_CUDA;
 
-  const int n_vtiles = (a.vocab + BN - 1) / BN;
-  const int n_vgroups = std::max(1, std::min(sms / n_mtiles, n_vtiles));
+  const int n_quanta = (a.vocab + BQ - 1) / BQ;
+  const int n_vgroups = std::max(1, std::min(sms / n_mtiles, n_quanta));
   const int grid = n_mtiles * n_vgroups;
 
-  // V: dim0 = rank (contiguous), dim1 = vocab; 64 x 256 boxes, 128-B swizzle
+  // V: dim0 = rank (contiguous), dim1 = vocab; 64 x 64 boxes, 128-B swizzle
   CUtensorMap tmV, tmL;
   {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.rank),
                           static_cast<cuuint64_t>(a.vocab)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.rank) * 2};
-    cuuint32_t box[2] = {BK, BN};
+    cuuint32_t box[2] = {BK, BQ};
     cuuint32_t es[2] = {1, 1};
     if (enc(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.V),
             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -542,13 +632,12 @@ dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream) {
   }
 
   uint8_t *ws = static_cast<uint8_t *>(a.workspace);
-  uint32_t *status = reinterpret_cast<uint32_t *>(ws + kStatusOffset);
-  uint32_t *counters = reinterpret_cast<uint32_t *>(ws + kChainCounterOffset);
-  unsigned long long *slots =
-      reinterpret_cast<unsigned long long *>(ws + kChainSlotsOffset);
-  const size_t clear_bytes = kChainSlotsOffset - kChainCounterOffset +
-                             static_cast<size_t>(a.N) * a.K * 8;
-  if (cudaMemsetAsync(counters, 0, clear_bytes, stream) != cudaSuccess)
+  // everything after the status word is per-call state: clear it
+  const size_t clear_bytes = chain_counters_offset(a.N, a.K) +
+                             static_cast<size_t>(n_mtiles) * a.K * 4 -
+                             kChainAbortOffset;
+  if (cudaMemsetAsync(ws + kChainAbortOffset, 0, clear_bytes, stream) !=
+      cudaSuccess)
     return DSPARK_ERR_CUDA;
 
   ChainParams p;
@@ -556,37 +645,41 @@ dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream) {
   p.last_token = a.last_token;
   p.draft = a.draft;
   p.score = a.score;
-  p.status = status;
+  p.slots = reinterpret_cast<unsigned long long *>(ws + kChainSlotsOffset);
+  p.counters = reinterpret_cast<uint32_t *>(ws + chain_counters_offset(a.N, a.K));
+  p.g_abort = reinterpret_cast<uint32_t *>(ws + kChainAbortOffset);
+  p.status = reinterpret_cast<uint32_t *>(ws + kStatusOffset);
   p.N = a.N;
   p.K = a.K;
   p.vocab = a.vocab;
   p.rank = a.rank;
   p.n_mtiles = n_mtiles;
   p.n_vgroups = n_vgroups;
-  p.n_vtiles = n_vtiles;
+  p.n_quanta = n_quanta;
   p.l_k_is_dim1 = l_k_is_dim1;
-
-  for (int k = 0; k < a.K; ++k) {
-    p.k_pos = k;
-    p.slots = slots + static_cast<size_t>(k) * a.N;
-    p.counter = counters + k;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(CHAIN_THREADS);
-    cfg.dynamicSmemBytes = CHAIN_SMEM_BYTES;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = k > 0 ? 1 : 0;  // position 0 waits for all prior work
-    cudaError_t e;
-    if (a.logits_dtype == DSPARK_BF16)
-      e = cudaLaunchKernelEx(&cfg, chain_position_kernel<DSPARK_BF16>, tmV, tmL, p);
-    else
-      e = cudaLaunchKernelEx(&cfg, chain_position_kernel<DSPARK_F32>, tmV, tmL, p);
-    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+  {
+    const double v_bytes = static_cast<double>(a.vocab) * a.rank * 2;
+    const int tenths = static_cast<int>(10.0 * kL2KeepBytes / v_bytes);
+    p.v_keep_tenths = std::max(0, std::min(10, tenths));
   }
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(CHAIN_THREADS);
+  cfg.dynamicSmemBytes = CHAIN_SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs co-resident
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (a.logits_dtype == DSPARK_BF16)
+    e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_BF16>, tmV, tmL, p);
+  else
+    e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_F32>, tmV, tmL, p);
+  if (e == cudaErrorCooperativeLaunchTooLarge) return DSPARK_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }
 

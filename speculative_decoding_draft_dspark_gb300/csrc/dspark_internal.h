@@ -11,8 +11,9 @@ namespace dspark {
 
 // workspace layout (bytes from the workspace base)
 constexpr size_t kStatusOffset = 0;         // uint32 sticky status word
-constexpr size_t kChainCounterOffset = 64;  // uint32 [K <= 32] CTA counters
-constexpr size_t kChainSlotsOffset = 256;   // uint64 [K][N] per-row winners
+constexpr size_t kChainAbortOffset = 4;     // uint32 chain abort flag
+constexpr size_t kChainSlotsOffset = 256;   // uint64 [K][N] per-row winners,
+                                            // then uint32 [K][N/128] counters
 constexpr size_t kSelectWorkspaceBytes = 256;
 
 constexpr int kMaxK = 32;

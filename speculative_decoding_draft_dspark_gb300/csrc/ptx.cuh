@@ -85,6 +85,39 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// L2 policy: a fraction (tenths, 0..10) of the lines get evict_last, the
+// rest evict_first; the split is by address, so the same lines stay
+// protected on every access
+__device__ __forceinline__ uint64_t policy_keep_tenths(int tenths) {
+  uint64_t p;
+  switch (tenths) {
+#define DSPARK_KEEP_CASE(t, f)                                              \
+  case t:                                                                  \
+    asm volatile(                                                          \
+        "createpolicy.fractional.L2::evict_last.L2::evict_first.b64 %0, " f \
+        ";"                                                                \
+        : "=l"(p));                                                        \
+    break;
+    DSPARK_KEEP_CASE(1, "0.1")
+    DSPARK_KEEP_CASE(2, "0.2")
+    DSPARK_KEEP_CASE(3, "0.3")
+    DSPARK_KEEP_CASE(4, "0.4")
+    DSPARK_KEEP_CASE(5, "0.5")
+    DSPARK_KEEP_CASE(6, "0.6")
+    DSPARK_KEEP_CASE(7, "0.7")
+    DSPARK_KEEP_CASE(8, "0.8")
+    DSPARK_KEEP_CASE(9, "0.9")
+#undef DSPARK_KEEP_CASE
+    case 0:
+      p = policy_evict_first();
+      break;
+    default:
+      p = policy_evict_last();
+      break;
+  }
+  return p;
+}
+
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m,
                                             uint64_t *bar, int32_t c0,
                                             int32_t c1, uint64_t policy) {
@@ -220,6 +253,18 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
         "+r"(r[30]), "+r"(r[31])
       :
       : "memory");
+}
+
+// --------------------------------------------- grid-level synchronisation
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// barrier among `count` threads of the CTA (ids 1..15; 0 is __syncthreads)
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ------------------------------------------- programmatic dependent launch
