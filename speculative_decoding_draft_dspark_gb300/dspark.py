@@ -48,6 +48,9 @@ _SIGS = {
     "dspark_chain_workspace_size": (_SZ, [_I32, _I32]),
     "dspark_chain_draft": (_I32, [_P, _I32, _I64, _I64, _P, _P, _P, _I32, _I32,
                                   _I32, _I32, _P, _P, _P, _SZ, _P]),
+    "dspark_chain_draft_noalloc": (_I32, [_P, _I32, _I64, _I64, _P, _P, _P,
+                                          _I32, _I32, _I32, _I32, _P, _P, _P,
+                                          _P]),
     "dspark_select_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "dspark_survival_topb": (_I32, [_P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P,
                                     _SZ, _P]),
@@ -150,6 +153,31 @@ def dspark_chain_draft(logits, U, V, last_token, draft_tokens, draft_score,
         _ptr(draft_score), _ptr(workspace), _nbytes(workspace),
         _stream(stream))
     return _check("dspark_chain_draft", code, raise_on_error)
+
+
+def dspark_chain_draft_noalloc(logits, U, V, last_token, draft_tokens,
+                               draft_score, device_status=None, *, N=None,
+                               K=None, vocab=None, rank=None, stride_n=None,
+                               stride_k=None, logits_dtype=None, stream=None,
+                               raise_on_error=True) -> int:
+    """dspark_chain_draft without a workspace, for callers that cannot
+    allocate device memory (scratch lives in the library's own fixed device
+    array; see include/dspark.h).  device_status: optional uint32 device
+    tensor that receives this call's status bits."""
+    import torch
+    if logits_dtype is None:
+        logits_dtype = BF16 if logits.dtype == torch.bfloat16 else F32
+    N = logits.shape[0] if N is None else N
+    K = logits.shape[1] if K is None else K
+    vocab = logits.shape[2] if vocab is None else vocab
+    rank = U.shape[1] if rank is None else rank
+    stride_n = logits.stride(0) if stride_n is None else stride_n
+    stride_k = logits.stride(1) if stride_k is None else stride_k
+    code = load().dspark_chain_draft_noalloc(
+        _ptr(logits), logits_dtype, stride_n, stride_k, _ptr(U), _ptr(V),
+        _ptr(last_token), N, K, vocab, rank, _ptr(draft_tokens),
+        _ptr(draft_score), _ptr(device_status), _stream(stream))
+    return _check("dspark_chain_draft_noalloc", code, raise_on_error)
 
 
 # -------------------------------------------------------------- scheduler
