@@ -36,7 +36,7 @@ METRIC = ("µs per draft-chain+schedule step at batch 256, K=7, vocab "
 WORKLOAD = "headline"
 CHAIN_SRC = os.path.join(ROOT, "speculative_decoding_draft_dspark_gb300",
                          "csrc", "chain.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "chain_position_headline_ncu.md")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "chain_kernel_headline_ncu.md")
 
 
 def parse_args():
@@ -62,19 +62,18 @@ def dist_env():
 
 
 def algorithmic_bytes_per_launch(cfg) -> float:
-    """Minimum HBM bytes of one chain launch (one draft position): the
-    position's logits slice, V read once per step (amortised over the K
-    launches), the gathered U rows and the token reads/writes."""
+    """Minimum HBM bytes of one chain launch (all K draft positions): every
+    logits element once, V once, the gathered U rows and the tokens."""
     esz = 2 if cfg.logits_dtype == "bf16" else 4
-    logits = cfg.N * cfg.vocab * esz
-    v_once = cfg.vocab * cfg.rank * 2 / cfg.K
-    u_rows = cfg.N * cfg.rank * 2
-    tokens = cfg.N * 4 * 2
+    logits = cfg.N * cfg.K * cfg.vocab * esz
+    v_once = cfg.vocab * cfg.rank * 2
+    u_rows = cfg.N * cfg.K * cfg.rank * 2
+    tokens = cfg.N * cfg.K * 4 * 2
     return logits + v_once + u_rows + tokens
 
 
 def flops_per_launch(cfg) -> float:
-    return 2.0 * cfg.N * cfg.vocab * cfg.rank
+    return 2.0 * cfg.N * cfg.K * cfg.vocab * cfg.rank
 
 
 def measured_peaks():
@@ -298,7 +297,7 @@ def run_gpu(args):
     value_us = ms_per_iter * 1e3 / world   # job-wide microseconds per step
     hbm, tf_burst, tf_sus, peak_src = measured_peaks()
     chain_med = statistics.median(chain_us)
-    per_launch_s = chain_med * 1e-6 / cfg.K
+    per_launch_s = chain_med * 1e-6  # the chain is one launch per step
     achieved_gbs = algorithmic_bytes_per_launch(cfg) / per_launch_s / 1e9
     achieved_tf = flops_per_launch(cfg) / per_launch_s / 1e12
     traffic = recorded_traffic()
@@ -330,7 +329,7 @@ def run_gpu(args):
             "host_clock_us_per_step": round(t_host * 1e6 / K_steps, 3),
         },
         "roofline": {
-            "bound": "hbm", "kernel": "chain_position_kernel (per launch = one position)",
+            "bound": "hbm", "kernel": "chain_kernel (one launch = all K positions)",
             "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(achieved_gbs / hbm, 4), "traffic": traffic,
             "algorithmic_bytes_per_launch": algorithmic_bytes_per_launch(cfg),
@@ -343,7 +342,7 @@ def run_gpu(args):
             "frac_of_sustained": round(achieved_tf / tf_sus, 4),
             "flops_per_launch": flops_per_launch(cfg),
         },
-        "gpu_launches": K_steps * (cfg.K + 1),
+        "gpu_launches": K_steps * 2,   # chain_kernel + select_kernel per step
         "clocks": clocks,
     }
     if rank == 0:
