@@ -50,6 +50,9 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-graph", action="store_true",
                     help="launch eagerly instead of replaying CUDA graphs")
+    ap.add_argument("--serial", action="store_true",
+                    help="run the scheduler after the chain on one stream "
+                         "instead of alongside it")
     return ap.parse_args()
 
 
@@ -212,6 +215,16 @@ class Step:
                                   self.pre, self.ne, self.ns, self.B, self.obj,
                                   self.ln, self.cu, self.vi, self.vt, self.sws)
 
+    def select_nodraft(self):
+        """The scheduler without the draft (verify_tok filled by gather)."""
+        self.D.dspark_select_step(self.conf, self.mask, self.cost, self.T, 0.0,
+                                  self.flags, None, self.surv, self.srt,
+                                  self.pre, self.ne, self.ns, self.B, self.obj,
+                                  self.ln, self.cu, self.vi, None, self.sws)
+
+    def gather(self):
+        self.D.dspark_gather_verify_tokens(self.vi, self.B, self.draft, self.vt)
+
 
 def run_gpu(args):
     import numpy as np
@@ -232,6 +245,9 @@ def run_gpu(args):
     D = st.D
     stream = torch.cuda.Stream(device=dev)
 
+    side = torch.cuda.Stream(device=dev)
+    serial = args.serial
+
     # eager warm-up (also sets the kernels' shared-memory attributes)
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -240,23 +256,63 @@ def run_gpu(args):
     stream.synchronize()
     assert D.dspark_read_status(st.cws) == 0 and D.dspark_read_status(st.sws) == 0
 
+    # the three parts of a step: chain (main stream), scheduler (side stream
+    # alongside the chain, or main stream after it when --serial) and the
+    # verify-token gather after the join
     if args.no_graph:
-        run_chain, run_select = st.chain, st.select
+        run_chain = st.chain
+        run_select = st.select if serial else st.select_nodraft
+        run_gather = st.gather
     else:
-        g_chain, g_sel = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        g_chain, g_sel, g_gat = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
+                                 torch.cuda.CUDAGraph())
         with torch.cuda.graph(g_chain, stream=stream):
             st.chain()
-        with torch.cuda.graph(g_sel, stream=stream):
-            st.select()
-        run_chain, run_select = g_chain.replay, g_sel.replay
+        with torch.cuda.graph(g_sel, stream=side if not serial else stream):
+            if serial:
+                st.select()
+            else:
+                st.select_nodraft()
+        with torch.cuda.graph(g_gat, stream=stream):
+            st.gather()
+        run_chain, run_select, run_gather = g_chain.replay, g_sel.replay, g_gat.replay
+
+    def step(e=None):
+        if serial:
+            if e is not None:
+                e[0].record(stream)
+            with torch.cuda.stream(stream):
+                run_chain()
+            if e is not None:
+                e[1].record(stream)
+            with torch.cuda.stream(stream):
+                run_select()
+            if e is not None:
+                e[2].record(stream)
+                e[3].record(stream)
+            return
+        fork = e[0] if e is not None else torch.cuda.Event()
+        fork.record(stream)
+        side.wait_event(fork)
+        with torch.cuda.stream(stream):
+            run_chain()
+        if e is not None:
+            e[1].record(stream)
+        with torch.cuda.stream(side):
+            run_select()
+        joined = e[2] if e is not None else torch.cuda.Event()
+        joined.record(side)
+        stream.wait_event(joined)
+        with torch.cuda.stream(stream):
+            run_gather()
+        if e is not None:
+            e[3].record(stream)
 
     K_steps, W = args.steps, args.warmup
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K_steps)]
-    with torch.cuda.stream(stream):
-        for _ in range(W):
-            run_chain()
-            run_select()
-    stream.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K_steps)]
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
     if world > 1:
@@ -267,15 +323,10 @@ def run_gpu(args):
     t_host0 = time.perf_counter()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for i in range(K_steps):
-            ev[i][0].record(stream)
-            run_chain()
-            ev[i][1].record(stream)
-            run_select()
-            ev[i][2].record(stream)
-        end.record(stream)
+    start.record(stream)
+    for i in range(K_steps):
+        step(ev[i])
+    end.record(stream)
     torch.cuda.synchronize()
     t_host = time.perf_counter() - t_host0
     if world > 1:
@@ -283,8 +334,11 @@ def run_gpu(args):
     clocks = sampler.stop()
     total_ms = start.elapsed_time(end)
     chain_us = [ev[i][0].elapsed_time(ev[i][1]) * 1e3 for i in range(K_steps)]
-    sel_us = [ev[i][1].elapsed_time(ev[i][2]) * 1e3 for i in range(K_steps)]
-    step_us = [ev[i][0].elapsed_time(ev[i][2]) * 1e3 for i in range(K_steps)]
+    if serial:
+        sel_us = [ev[i][1].elapsed_time(ev[i][2]) * 1e3 for i in range(K_steps)]
+    else:  # the scheduler starts with the chain
+        sel_us = [ev[i][0].elapsed_time(ev[i][2]) * 1e3 for i in range(K_steps)]
+    step_us = [ev[i][0].elapsed_time(ev[i][3]) * 1e3 for i in range(K_steps)]
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -315,8 +369,10 @@ def run_gpu(args):
                         f"{cfg.vocab}, rank {cfg.rank}, bf16 logits/U/V, "
                         f"{cfg.n_nonsampling} chunked-prefill requests, T={cfg.T}, "
                         f"cost table L={cfg.L} stepped to 4096",
-            "timing": "CUDA graphs (chain, select) replayed; CUDA events on "
-                      "the launching stream",
+            "timing": ("CUDA graphs replayed; " + ("scheduler after the chain "
+                       "on one stream" if serial else "scheduler on a second "
+                       "stream alongside the chain, verify-token gather after "
+                       "the join") + "; CUDA events on the launching streams"),
             "l2": "inputs larger than L2 (logits 939.5 MB, V 134.2 MB); no flush",
             "parallelism": f"replicas x{world}",
         },
@@ -342,7 +398,8 @@ def run_gpu(args):
             "frac_of_sustained": round(achieved_tf / tf_sus, 4),
             "flops_per_launch": flops_per_launch(cfg),
         },
-        "gpu_launches": K_steps * 2,   # chain_kernel + select_kernel per step
+        # chain_kernel + select_kernel (+ gather_verify_kernel) per step
+        "gpu_launches": K_steps * (2 if serial else 3),
         "clocks": clocks,
     }
     if rank == 0:

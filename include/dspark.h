@@ -240,6 +240,17 @@ DSPARK_API dspark_status dspark_select_step(
     int32_t *verify_tok,
     void *workspace, size_t workspace_bytes, dspark_stream_t stream);
 
+/* Verify tokens of the compacted list: verify_tok[j] = draft_tokens[
+ * verify_idx[j]] for j < *B (B and verify_idx as written by the scheduler).
+ * The scheduler does not depend on the draft except for these tokens, so a
+ * caller can run dspark_select_step (with draft_tokens = NULL) on a second
+ * stream while dspark_chain_draft runs, join the streams, then call this;
+ * dspark_chain_draft leaves an SM idle for that when it costs at most 1/64
+ * of its CTAs.  Limits as for the scheduler calls. */
+DSPARK_API dspark_status dspark_gather_verify_tokens(
+    const int32_t *verify_idx, const int32_t *B, const int32_t *draft_tokens,
+    int32_t N, int32_t K, int32_t *verify_tok, dspark_stream_t stream);
+
 /* Cost-table preparation.  "Adaptive Verification in vLLM", "The cost model":
  * profiling noise is removed by forcing the curve monotone; run once per
  * table.  mode = DSPARK_COST_FORCE_MONOTONE (running max from the left) or

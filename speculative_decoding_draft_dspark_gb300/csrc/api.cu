@@ -274,6 +274,19 @@ dspark_status dspark_select_step(
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
+dspark_status dspark_gather_verify_tokens(const int32_t *verify_idx,
+                                         const int32_t *B,
+                                         const int32_t *draft_tokens, int32_t N,
+                                         int32_t K, int32_t *verify_tok,
+                                         dspark_stream_t stream) {
+  dspark_status s = check_select_dims(N, K);
+  if (s != DSPARK_OK) return s;
+  if (!verify_idx || !B || !draft_tokens || !verify_tok)
+    return DSPARK_ERR_INVALID_ARG;
+  return gather_verify_launch(verify_idx, B, draft_tokens, N * K, verify_tok,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
 dspark_status dspark_force_monotone(const float *cost_in, float *cost_out,
                                     int32_t cost_len, uint32_t mode,
                                     dspark_stream_t stream) {

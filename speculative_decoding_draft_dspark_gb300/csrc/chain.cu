@@ -585,7 +585,17 @@ dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream) {
   if (ensure_kernel_attrs(dev) != cudaSuccess) return DSPARK_ERR_CUDA;
 
   const int n_quanta = (a.vocab + BQ - 1) / BQ;
-  const int n_vgroups = std::max(1, std::min(sms / n_mtiles, n_quanta));
+  // Leave at least one SM idle when that costs at most 1/64 of the CTAs, so
+  // independent work (the scheduler on another stream) can run alongside the
+  // chain instead of after it; the chain is HBM-bound, so the CTA it gives
+  // up costs next to nothing.
+  int groups = sms / n_mtiles;
+  if (n_mtiles * groups == sms && groups > 1) {
+    const int fewer = (sms - 1) / n_mtiles;
+    if (static_cast<long long>(n_mtiles) * (groups - fewer) * 64 <= sms)
+      groups = fewer;
+  }
+  const int n_vgroups = std::max(1, std::min(groups, n_quanta));
   const int grid = n_mtiles * n_vgroups;
 
   // V: dim0 = rank (contiguous), dim1 = vocab; 64 x 64 boxes, 128-B swizzle

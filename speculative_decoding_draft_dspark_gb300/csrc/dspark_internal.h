@@ -76,6 +76,10 @@ enum SelectStage : uint32_t {
 
 dspark_status select_launch(const SelectArgs &a, uint32_t stages,
                             cudaStream_t stream);
+dspark_status gather_verify_launch(const int32_t *verify_idx,
+                                   const int32_t *B_dev, const int32_t *draft,
+                                   int32_t NK, int32_t *verify_tok,
+                                   cudaStream_t stream);
 dspark_status force_monotone_launch(const float *in, float *out, int32_t L,
                                     uint32_t mode, cudaStream_t stream);
 

@@ -654,6 +654,21 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   }
 }
 
+// verify_tok[j] = draft[verify_idx[j]] for j < *B (after the chain has
+// finished, when the scheduler ran alongside it without the draft)
+__global__ void __launch_bounds__(256)
+    gather_verify_kernel(const int32_t *verify_idx, const int32_t *B_dev,
+                         const int32_t *draft, const int NK,
+                         int32_t *verify_tok) {
+  int B = *B_dev;
+  B = B < 0 ? 0 : (B > NK ? NK : B);
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < B;
+       j += gridDim.x * blockDim.x) {
+    const int idx = verify_idx[j];
+    verify_tok[j] = (idx >= 0 && idx < NK) ? draft[idx] : 0;
+  }
+}
+
 // ==========================================================================
 // host side
 // ==========================================================================
@@ -694,6 +709,16 @@ dspark_status select_launch(const SelectArgs &a, uint32_t stages,
   }
   dyn = (dyn + 15) & ~static_cast<size_t>(15);
   select_kernel<<<1, SEL_THREADS, dyn, stream>>>(a, stages, P2);
+  return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+dspark_status gather_verify_launch(const int32_t *verify_idx,
+                                   const int32_t *B_dev, const int32_t *draft,
+                                   int32_t NK, int32_t *verify_tok,
+                                   cudaStream_t stream) {
+  const int blocks = (NK + 255) / 256 < 8 ? (NK + 255) / 256 : 8;
+  gather_verify_kernel<<<blocks, 256, 0, stream>>>(verify_idx, B_dev, draft, NK,
+                                                   verify_tok);
   return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 

@@ -62,6 +62,7 @@ _SIGS = {
     "dspark_select_step": (_I32, [_P, _P, _I32, _I32, _P, _I32, _P, _F, _U32,
                                   _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                   _P, _P, _SZ, _P]),
+    "dspark_gather_verify_tokens": (_I32, [_P, _P, _P, _I32, _I32, _P, _P]),
     "dspark_force_monotone": (_I32, [_P, _P, _I32, _U32, _P]),
     "dspark_read_status": (_I32, [_P, _P, _P]),
     "dspark_clear_status": (_I32, [_P, _P]),
@@ -238,6 +239,15 @@ def dspark_select_step(conf, sampling_mask, cost, T_dev, draft_cost, flags,
         _ptr(cu_len), _ptr(verify_idx), _ptr(verify_tok), _ptr(workspace),
         _nbytes(workspace), _stream(stream))
     return _check("dspark_select_step", code, raise_on_error)
+
+
+def dspark_gather_verify_tokens(verify_idx, B, draft_tokens, verify_tok, *,
+                                stream=None, raise_on_error=True) -> int:
+    N, K = draft_tokens.shape
+    code = load().dspark_gather_verify_tokens(
+        _ptr(verify_idx), _ptr(B), _ptr(draft_tokens), N, K, _ptr(verify_tok),
+        _stream(stream))
+    return _check("dspark_gather_verify_tokens", code, raise_on_error)
 
 
 def dspark_force_monotone(cost_in, cost_out, mode=COST_FORCE_MONOTONE, *,

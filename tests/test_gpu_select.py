@@ -135,3 +135,59 @@ def test_tiny_survivals_exact_sums():
     conf[:4, :] = 1e-30
     cost = (5 + 0.001 * np.arange(4096)).astype(np.float32)
     _both(conf, None, cost, 1)
+
+
+def test_scheduler_alongside_chain_then_gather():
+    """The scheduler runs on a second stream while the chain runs, without
+    the draft; after the join dspark_gather_verify_tokens fills the verify
+    tokens.  Results equal the oracle's serial step."""
+    import torch
+    from gpu_harness import up, up_bf16, i32
+    from speculative_decoding_draft_dspark_gb300 import dspark as D
+    cfg = workloads.get_config("dsv4")
+    sel = workloads.make_select_inputs(cfg)
+    fac = workloads.make_chain_factors(cfg)
+    logits = workloads.make_logits_rows(cfg)
+    last = workloads.make_last_token(cfg)
+    N, K = cfg.N, cfg.K
+    d_logits = up(logits.view(np.int16)).view(torch.bfloat16)
+    draft = torch.zeros(N, K, dtype=torch.int32, device="cuda")
+    cws = D.new_workspace(D.dspark_chain_workspace_size(N, K))
+    conf, mask, cost = up(sel["conf"]), up(sel["mask"]), up(sel["cost"])
+    T = up(np.array([sel["T"]], np.int32))
+    surv = torch.zeros(N, K, dtype=torch.float32, device="cuda")
+    srt, pre = i32(N * K), torch.zeros(N * K + 1, dtype=torch.float64, device="cuda")
+    ne, ns, B = i32(1), i32(1), i32(1)
+    obj = torch.zeros(1, dtype=torch.float64, device="cuda")
+    ln, cu, vi, vt = i32(N), i32(N + 1), i32(N * K), i32(N * K)
+    sws = D.new_workspace(D.dspark_select_workspace_size(N, K, cost.numel()))
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    fork = torch.cuda.Event()
+    fork.record(main)
+    side.wait_event(fork)
+    D.dspark_chain_draft(d_logits, up_bf16(fac["U"]), up_bf16(fac["V"]),
+                         up(last), draft, None, cws)
+    with torch.cuda.stream(side):
+        D.dspark_select_step(conf, mask, cost, T, 0.0, 0, None, surv, srt, pre,
+                             ne, ns, B, obj, ln, cu, vi, None, sws)
+    join = torch.cuda.Event()
+    join.record(side)
+    main.wait_event(join)
+    D.dspark_gather_verify_tokens(vi, B, draft, vt)
+    torch.cuda.synchronize()
+    ch = oracle.chain(logits, "bf16", fac["U"], fac["V"], last)
+    dg = draft.cpu().numpy()
+    r = oracle.select_step(sel["conf"], sel["mask"], sel["cost"], sel["T"],
+                           draft=ch["draft"])
+    Bg = int(B.item())
+    assert Bg == r["B"]
+    got_idx = vi.cpu().numpy()[:Bg]
+    np.testing.assert_array_equal(got_idx, r["verify_idx"])
+    # tokens: equal to the oracle's wherever the drafts agree (everywhere
+    # outside fp32 near-ties), and always the device's own draft tokens
+    same = dg.reshape(-1)[got_idx] == ch["draft"].reshape(-1)[got_idx]
+    assert same.mean() > 0.999
+    got_tok = vt.cpu().numpy()[:Bg]
+    np.testing.assert_array_equal(got_tok[same], r["verify_tok"][same])
+    np.testing.assert_array_equal(got_tok, dg.reshape(-1)[got_idx])
