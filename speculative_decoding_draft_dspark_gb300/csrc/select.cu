@@ -181,6 +181,9 @@ __device__ __forceinline__ Acc256 shfl_up(const Acc256 &v, int o) {
 struct OpAddInt {
   __device__ int operator()(int a, int b) const { return a + b; }
 };
+struct OpMinInt {
+  __device__ int operator()(int a, int b) const { return a < b ? a : b; }
+};
 struct OpMaxNan {
   __device__ float operator()(float a, float b) const { return fmax_nan(a, b); }
 };
@@ -363,10 +366,120 @@ __device__ __forceinline__ double f64_from_key(unsigned long long k) {
 }
 
 // ------------------------------------------------------------------------
+// bitonic sort of P2 (key, slot) pairs in shared memory into priority order
+// (larger key first, then smaller slot).  Thread t holds elements
+// [t*E, t*E+E) in registers: strides below E are compare-exchanges inside a
+// thread, strides below 32*E exchange with a lane of the same warp, only
+// larger strides go through shared memory (one barrier each).
+// ------------------------------------------------------------------------
+__device__ __forceinline__ bool prio_first(unsigned long long ka, uint32_t sa,
+                                           unsigned long long kb, uint32_t sb) {
+  return ka > kb || (ka == kb && sa < sb);
+}
+
+template <int E>
+__device__ void block_bitonic(unsigned long long *keys, uint16_t *sidx,
+                              const int P2) {
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const bool active = tid < P2 / E;  // whole warps (P2 / E is a multiple of 32)
+  unsigned long long k[E];
+  uint32_t v[E];
+  if (active) {
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      k[j] = keys[tid * E + j];
+      v[j] = sidx[tid * E + j];
+    }
+  }
+  for (int s = 2; s <= P2; s <<= 1) {
+    int d = s >> 1;
+    if (d >= 32 * E) {  // shared-memory passes
+      if (active) {
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+          keys[tid * E + j] = k[j];
+          sidx[tid * E + j] = static_cast<uint16_t>(v[j]);
+        }
+      }
+      __syncthreads();
+      for (; d >= 32 * E; d >>= 1) {
+        for (int i = tid; i < (P2 >> 1); i += blockDim.x) {
+          const int lo = ((i & ~(d - 1)) << 1) | (i & (d - 1));
+          const int hi = lo + d;
+          const unsigned long long ka = keys[lo], kb = keys[hi];
+          const uint16_t ia = sidx[lo], ib = sidx[hi];
+          const bool up = (lo & s) == 0;
+          if (up != prio_first(ka, ia, kb, ib)) {
+            keys[lo] = kb;
+            keys[hi] = ka;
+            sidx[lo] = ib;
+            sidx[hi] = ia;
+          }
+        }
+        __syncthreads();
+      }
+      if (active) {
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+          k[j] = keys[tid * E + j];
+          v[j] = sidx[tid * E + j];
+        }
+      }
+    }
+    if (active) {
+      for (; d >= E; d >>= 1) {  // partner in the same warp
+        const int m = d / E;
+        const bool lower = (lane & m) == 0;
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+          const int i = tid * E + j;
+          const unsigned long long pk = __shfl_xor_sync(0xFFFFFFFFu, k[j], m);
+          const uint32_t pv = __shfl_xor_sync(0xFFFFFFFFu, v[j], m);
+          const bool keep_first = lower == ((i & s) == 0);
+          if (keep_first != prio_first(k[j], v[j], pk, pv)) {
+            k[j] = pk;
+            v[j] = pv;
+          }
+        }
+      }
+#pragma unroll
+      for (int dd = E / 2; dd >= 1; dd >>= 1) {  // partner in this thread
+        if (dd > d) continue;
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+          if (j & dd) continue;
+          const int jj = j | dd;
+          const int i = tid * E + j;
+          const bool up = (i & s) == 0;
+          if (up != prio_first(k[j], v[j], k[jj], v[jj])) {
+            const unsigned long long tk = k[j];
+            const uint32_t tv = v[j];
+            k[j] = k[jj];
+            v[j] = v[jj];
+            k[jj] = tk;
+            v[jj] = tv;
+          }
+        }
+      }
+    }
+  }
+  if (active) {
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      keys[tid * E + j] = k[j];
+      sidx[tid * E + j] = static_cast<uint16_t>(v[j]);
+    }
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------------
 // the scheduler kernel
 // ------------------------------------------------------------------------
 constexpr int kMaxChunk = (kMaxSlots + 1 + SEL_THREADS - 1) / SEL_THREADS + 1;
 
+template <int E>
 __global__ void __launch_bounds__(SEL_THREADS, 1)
     select_kernel(const SelectArgs a, const uint32_t stages, const int P2) {
   extern __shared__ __align__(16) uint8_t dsm[];
@@ -420,26 +533,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     n_s = block_reduce(my_ns, OpAddInt(), 0, sh_int);
     S = n_s * K;
 
-    // bitonic network: priority = larger key, then smaller slot id
-    for (int size = 2; size <= P2; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = tid; i < (P2 >> 1); i += NT) {
-          const int lo = ((i & ~(stride - 1)) << 1) | (i & (stride - 1));
-          const int hi = lo + stride;
-          const unsigned long long ka = keys[lo], kb = keys[hi];
-          const uint16_t ia = sidx[lo], ib = sidx[hi];
-          const bool a_first = ka > kb || (ka == kb && ia < ib);
-          const bool up = (lo & size) == 0;
-          if (up != a_first) {
-            keys[lo] = kb;
-            keys[hi] = ka;
-            sidx[lo] = ib;
-            sidx[hi] = ia;
-          }
-        }
-        __syncthreads();
-      }
-    }
+    __syncthreads();
+    block_bitonic<E>(keys, sidx, P2);
     if (a.sorted_slots)
       for (int j = tid; j < S; j += NT) a.sorted_slots[j] = sidx[j];
     if (tid == 0) {
@@ -525,6 +620,34 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
       }
       const double dc = static_cast<double>(a.draft_cost);
       const double ns = static_cast<double>(n_s);
+      // P_b of the chunk's points
+      double Pl[kMaxChunk + 1];
+      for (int i = 0; i < cnt; ++i) {
+        const int b = b0 + i;
+        Pl[i] = b == 0 ? 0.0 : (fused_order ? Pd[b - 1] : a.prefix_in[b]);
+      }
+      const bool greedy = (a.flags & DSPARK_BUDGET_GREEDY_STOP) != 0;
+      // f(b) = fl(fl(N_s + P_b) / fl(cost'[T+b] + draft_cost)) in fp64.  The
+      // fp64 divide is slow on this part, so the argmax first evaluates f in
+      // fp32 (relative error < 3e-7) and divides in fp64 only where the fp32
+      // value is within 1e-4 of the fp32 maximum: the fp64 maximiser, and
+      // every b tied with it, is always among those.  Denominators that are
+      // not normal positive fp32 numbers, or an fp32 overflow, send every b
+      // through fp64 instead.
+      float fa[kMaxChunk + 1];
+      bool fast = !greedy;
+      float amax = -INFINITY;
+      for (int i = 0; i < cnt; ++i) {
+        const float den32 = cf[i] + a.draft_cost;
+        if (!(den32 > 0.0f)) st |= DSPARK_DEV_COST_NONPOS;
+        const float num32 = static_cast<float>(Pl[i]) + static_cast<float>(n_s);
+        fa[i] = __fdiv_rn(num32, den32);
+        fast = fast && den32 >= 1.17549435e-38f && isfinite(fa[i]);
+        if (i < b1 - b0) amax = fmaxf(amax, fa[i]);
+      }
+      fast = block_reduce(fast ? 1 : 0, OpMinInt(), 1, sh_int) != 0;
+      if (fast) amax = block_reduce(amax, OpMaxNan(), -INFINITY, sh_f);
+      const float thr = amax - amax * 1e-4f;
       unsigned long long best_k = 0ull;
       int best_b = INT_MAX;
       int gstop = INT_MAX;
@@ -532,14 +655,9 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
       double f_prev = 0.0;
       for (int i = 0; i < cnt; ++i) {
         const int b = b0 + i;
-        double P;
-        if (b == 0)
-          P = 0.0;
-        else
-          P = fused_order ? Pd[b - 1] : a.prefix_in[b];
+        if (fast && !(fa[i] >= thr)) continue;
         const double den = __dadd_rn(static_cast<double>(cf[i]), dc);
-        if (!(den > 0.0)) st |= DSPARK_DEV_COST_NONPOS;
-        const double f = __ddiv_rn(__dadd_rn(ns, P), den);
+        const double f = __ddiv_rn(__dadd_rn(ns, Pl[i]), den);
         if (b < b1) {
           const unsigned long long k = f64_key(f);
           if (k > best_k || (k == best_k && b < best_b)) {
@@ -547,13 +665,15 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
             best_b = b;
           }
         }
-        if (i > 0 && gstop == INT_MAX && !(f > f_prev)) {
-          gstop = b - 1;
-          gval = f_prev;
+        if (greedy) {
+          if (i > 0 && gstop == INT_MAX && !(f > f_prev)) {
+            gstop = b - 1;
+            gval = f_prev;
+          }
+          f_prev = f;
         }
-        f_prev = f;
       }
-      if (a.flags & DSPARK_BUDGET_GREEDY_STOP) {
+      if (greedy) {
         // the objective at b_max for "never stopped"
         if (b1 == nb && b1 > b0 && gstop == INT_MAX) {
           gstop = INT_MAX - 1;  // marker: reached the end
@@ -681,6 +801,20 @@ static int next_pow2(int x) {
   return p;
 }
 
+template <int E>
+static cudaError_t set_select_attr() {
+  return cudaFuncSetAttribute(select_kernel<E>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              200 * 1024);
+}
+
+template <int E>
+static cudaError_t launch_select(const SelectArgs &a, uint32_t stages, int P2,
+                                 size_t dyn, cudaStream_t stream) {
+  select_kernel<E><<<1, SEL_THREADS, dyn, stream>>>(a, stages, P2);
+  return cudaGetLastError();
+}
+
 dspark_status select_launch(const SelectArgs &a, uint32_t stages,
                             cudaStream_t stream) {
   int dev = 0;
@@ -689,9 +823,11 @@ dspark_status select_launch(const SelectArgs &a, uint32_t stages,
   {
     std::lock_guard<std::mutex> lk(g_sel_mu);
     if (!g_sel_attr[dev]) {
-      if (cudaFuncSetAttribute(select_kernel,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               200 * 1024) != cudaSuccess)
+      if (set_select_attr<1>() != cudaSuccess ||
+          set_select_attr<2>() != cudaSuccess ||
+          set_select_attr<4>() != cudaSuccess ||
+          set_select_attr<8>() != cudaSuccess ||
+          set_select_attr<16>() != cudaSuccess)
         return DSPARK_ERR_CUDA;
       g_sel_attr[dev] = true;
     }
@@ -708,8 +844,18 @@ dspark_status select_launch(const SelectArgs &a, uint32_t stages,
     if (need > dyn) dyn = need;
   }
   dyn = (dyn + 15) & ~static_cast<size_t>(15);
-  select_kernel<<<1, SEL_THREADS, dyn, stream>>>(a, stages, P2);
-  return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+  // elements per thread of the sort: P2 / 1024, at least 1
+  const int E = P2 > SEL_THREADS ? P2 / SEL_THREADS : 1;
+  cudaError_t e;
+  switch (E) {
+    case 1: e = launch_select<1>(a, stages, P2, dyn, stream); break;
+    case 2: e = launch_select<2>(a, stages, P2, dyn, stream); break;
+    case 4: e = launch_select<4>(a, stages, P2, dyn, stream); break;
+    case 8: e = launch_select<8>(a, stages, P2, dyn, stream); break;
+    case 16: e = launch_select<16>(a, stages, P2, dyn, stream); break;
+    default: return DSPARK_ERR_UNSUPPORTED;
+  }
+  return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
 dspark_status gather_verify_launch(const int32_t *verify_idx,
