@@ -102,7 +102,12 @@ typedef int32_t dspark_status;
  * draft_score  optional out [N, K] fp32: the adjusted value at draft[n,k];
  *              NULL to skip.
  * workspace    >= dspark_chain_workspace_size(N, K) bytes, 256-byte aligned,
- *              zero-filled before its first use.
+ *              zero-filled before its first use.  Word 1 (bytes 4..7) is a
+ *              test hook: nonzero makes every barrier between positions wait
+ *              for one arrival more than can come, so the wait runs out after
+ *              its time limit and the call ends with DSPARK_DEV_TIMEOUT and
+ *              undefined drafts.  It exists to exercise the timeout path;
+ *              keep it zero.
  * Limits: 1 <= N <= 128 * (SM count), 1 <= K <= 32, 8 <= vocab < 2^31,
  * rank a multiple of 16 in [16, 256].
  * ------------------------------------------------------------------------ */

@@ -77,6 +77,7 @@ struct ChainParams {
   unsigned long long *slots;  // [K][N] per-row winners
   uint32_t *counters;         // [K][n_mtiles] epilogue warps done
   uint32_t *g_abort;          // set by any CTA that gives up
+  const uint32_t *hang_test;  // nonzero: barriers wait for one arrival too many
   uint32_t *status;
   int32_t N, K, vocab, rank;
   int32_t n_mtiles, n_vgroups, n_quanta;
@@ -129,7 +130,8 @@ __device__ __forceinline__ bool grid_wait(const ChainParams &p, int k,
                                           volatile uint32_t *cta_abort) {
   uint32_t r = 1;
   if ((threadIdx.x & 31) == 0) {
-    const uint32_t target = 4u * static_cast<uint32_t>(p.n_vgroups);
+    const uint32_t target = 4u * static_cast<uint32_t>(p.n_vgroups) +
+                            (*p.hang_test != 0u ? 1u : 0u);
     const uint32_t *cnt = &p.counters[k * p.n_mtiles + m_tile];
     if (ld_acquire_gpu(cnt) < target) {
       const uint64_t t0 = global_timer_ns();
@@ -658,6 +660,7 @@ dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream) {
   p.slots = reinterpret_cast<unsigned long long *>(ws + kChainSlotsOffset);
   p.counters = reinterpret_cast<uint32_t *>(ws + chain_counters_offset(a.N, a.K));
   p.g_abort = reinterpret_cast<uint32_t *>(ws + kChainAbortOffset);
+  p.hang_test = reinterpret_cast<const uint32_t *>(ws + kChainHangTestOffset);
   p.status = reinterpret_cast<uint32_t *>(ws + kStatusOffset);
   p.N = a.N;
   p.K = a.K;

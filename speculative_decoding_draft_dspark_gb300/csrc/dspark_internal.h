@@ -11,7 +11,8 @@ namespace dspark {
 
 // workspace layout (bytes from the workspace base)
 constexpr size_t kStatusOffset = 0;         // uint32 sticky status word
-constexpr size_t kChainAbortOffset = 4;     // uint32 chain abort flag
+constexpr size_t kChainHangTestOffset = 4;  // uint32 test hook (see dspark.h)
+constexpr size_t kChainAbortOffset = 8;     // uint32 chain abort flag
 constexpr size_t kChainSlotsOffset = 256;   // uint64 [K][N] per-row winners,
                                             // then uint32 [K][N/128] counters
 constexpr size_t kSelectWorkspaceBytes = 256;
