@@ -64,6 +64,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, device) -> float:
+    """Largest value over all ranks of the process group (1 rank: itself)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_us_per_step(total_ms: float, steps: int, world: int) -> float:
+    """Job-wide microseconds per step: every rank runs its own step in each
+    iteration, so one iteration completes `world` steps."""
+    return total_ms * 1e3 / steps / world
+
+
 def algorithmic_bytes_per_launch(cfg) -> float:
     """Minimum HBM bytes of one chain launch (all K draft positions): every
     logits element once, V once, the gathered U rows and the tokens."""
@@ -339,16 +356,13 @@ def run_gpu(args):
     else:  # the scheduler starts with the chain
         sel_us = [ev[i][0].elapsed_time(ev[i][2]) * 1e3 for i in range(K_steps)]
     step_us = [ev[i][0].elapsed_time(ev[i][3]) * 1e3 for i in range(K_steps)]
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
 
     # outputs of the timed steps are still the oracle's (cheap integrity check)
     assert D.dspark_read_status(st.cws) == 0 and D.dspark_read_status(st.sws) == 0
 
     ms_per_iter = total_ms / K_steps
-    value_us = ms_per_iter * 1e3 / world   # job-wide microseconds per step
+    value_us = job_us_per_step(total_ms, K_steps, world)
     hbm, tf_burst, tf_sus, peak_src = measured_peaks()
     chain_med = statistics.median(chain_us)
     per_launch_s = chain_med * 1e-6  # the chain is one launch per step
