@@ -250,8 +250,8 @@ DSPARK_API dspark_status dspark_select_step(
  * The scheduler does not depend on the draft except for these tokens, so a
  * caller can run dspark_select_step (with draft_tokens = NULL) on a second
  * stream while dspark_chain_draft runs, join the streams, then call this;
- * dspark_chain_draft leaves an SM idle for that when it costs at most 1/64
- * of its CTAs.  Limits as for the scheduler calls. */
+ * dspark_chain_draft always leaves at least one SM idle for that.  Limits
+ * as for the scheduler calls. */
 DSPARK_API dspark_status dspark_gather_verify_tokens(
     const int32_t *verify_idx, const int32_t *B, const int32_t *draft_tokens,
     int32_t N, int32_t K, int32_t *verify_tok, dspark_stream_t stream);

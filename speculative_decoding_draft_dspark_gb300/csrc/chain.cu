@@ -587,16 +587,11 @@ dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream) {
   if (ensure_kernel_attrs(dev) != cudaSuccess) return DSPARK_ERR_CUDA;
 
   const int n_quanta = (a.vocab + BQ - 1) / BQ;
-  // Leave at least one SM idle when that costs at most 1/64 of the CTAs, so
-  // independent work (the scheduler on another stream) can run alongside the
-  // chain instead of after it; the chain is HBM-bound, so the CTA it gives
-  // up costs next to nothing.
+  // Leave at least one SM idle so that independent work (the scheduler on
+  // another stream) runs alongside the chain instead of after it; the chain
+  // is HBM-bound, so the SMs it gives up cost next to nothing.
   int groups = sms / n_mtiles;
-  if (n_mtiles * groups == sms && groups > 1) {
-    const int fewer = (sms - 1) / n_mtiles;
-    if (static_cast<long long>(n_mtiles) * (groups - fewer) * 64 <= sms)
-      groups = fewer;
-  }
+  if (n_mtiles * groups > sms - 1 && groups > 1) groups = (sms - 1) / n_mtiles;
   const int n_vgroups = std::max(1, std::min(groups, n_quanta));
   const int grid = n_mtiles * n_vgroups;
 
