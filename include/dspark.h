@@ -256,6 +256,32 @@ DSPARK_API dspark_status dspark_gather_verify_tokens(
     const int32_t *verify_idx, const int32_t *B, const int32_t *draft_tokens,
     int32_t N, int32_t K, int32_t *verify_tok, dspark_stream_t stream);
 
+/* Greedy verification of the compacted list.  "DSpark on MAX", "The kernel
+ * pass", item 2: under greedy sampling a draft token is accepted iff it
+ * equals the target's best token; "How DSpark Speeds Up LLM Inference",
+ * "Context": the longest matching run is kept and the target adds its next
+ * token.
+ *
+ * target_logits [R, vocab] (logits_dtype), row r at r*row_stride elements
+ *               (16-byte aligned rows): each sampling request n has
+ *               draft_len[n] + 1 consecutive rows, request-major (the target's
+ *               outputs after the last committed token and after each of the
+ *               draft_len[n] verified draft tokens); R = cu_len[N] + N_sampling.
+ * draft_tokens [N, K], draft_len [N], cu_len [N+1], sampling_mask [N] (NULL =
+ *               all sample): as used and written by the scheduler.
+ * target_argmax out [N*(K+1)]: first-index argmax of each row (NaN ranks
+ *               highest; DSPARK_DEV_NAN_LOGIT is set in the workspace status).
+ * accepted, bonus out [N]: leading draft tokens equal to the target's argmax,
+ *               and the target's argmax after them; -1 for non-sampling
+ *               requests.
+ * workspace: a scheduler workspace (status word at offset 0). */
+DSPARK_API dspark_status dspark_greedy_verify(
+    const void *target_logits, int32_t logits_dtype, int64_t row_stride,
+    int32_t vocab, const int32_t *draft_tokens, const int32_t *draft_len,
+    const int32_t *cu_len, const uint8_t *sampling_mask, int32_t N, int32_t K,
+    int32_t *target_argmax, int32_t *accepted, int32_t *bonus,
+    void *workspace, size_t workspace_bytes, dspark_stream_t stream);
+
 /* Cost-table preparation.  "Adaptive Verification in vLLM", "The cost model":
  * profiling noise is removed by forcing the curve monotone; run once per
  * table.  mode = DSPARK_COST_FORCE_MONOTONE (running max from the left) or

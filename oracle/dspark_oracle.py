@@ -257,6 +257,48 @@ def compact(draft_len: np.ndarray, K: int, draft: np.ndarray | None = None) -> d
     return dict(cu_len=cu, verify_idx=idx, verify_tok=tok)
 
 
+# ---------------------------------------------------------------------------
+# greedy verification of the compacted list
+# ---------------------------------------------------------------------------
+def verify_rows(draft_len: np.ndarray, mask: np.ndarray) -> np.ndarray:
+    """First target row of every request: each sampling request has
+    draft_len[n] + 1 target rows (one per verified draft token plus the
+    bonus position), request-major; non-sampling requests have none."""
+    per = np.where(np.asarray(mask) != 0, np.asarray(draft_len) + 1, 0)
+    return np.concatenate([[0], np.cumsum(per)]).astype(np.int64)
+
+
+def greedy_verify(target_logits: np.ndarray, logits_dtype: str,
+                  draft: np.ndarray, draft_len: np.ndarray,
+                  mask: np.ndarray) -> dict:
+    """Compare-only acceptance ("DSpark on MAX", *The kernel pass*, item 2:
+    under greedy sampling a draft token is accepted iff it equals the
+    target's best token; "How DSpark Speeds Up LLM Inference", *Context*:
+    keep the longest matching run plus the target's next token).
+
+    target_logits: [R, vocab], R = sum over sampling requests of len + 1.
+    Returns the per-row target argmax (first index, NaN first), the accepted
+    length and the bonus token per request (-1 for non-sampling requests).
+    """
+    N, K = np.asarray(draft).shape
+    rows = verify_rows(draft_len, mask)
+    R = int(rows[-1])
+    tl = to_f64(target_logits[:R], logits_dtype)
+    tgt = np.argmax(tl, axis=1).astype(np.int64) if R else np.zeros(0, np.int64)
+    acc = np.full(N, -1, np.int64)
+    bonus = np.full(N, -1, np.int64)
+    for n in range(N):
+        if mask[n] == 0:
+            continue
+        r0, ln = int(rows[n]), int(draft_len[n])
+        a = 0
+        while a < ln and draft[n, a] == tgt[r0 + a]:
+            a += 1
+        acc[n] = a
+        bonus[n] = tgt[r0 + a]
+    return dict(target_argmax=tgt, accepted=acc, bonus=bonus, rows=rows)
+
+
 def select_step(conf, mask, cost, T, draft_cost=0.0, flags=0, draft=None) -> dict:
     """Survival -> order -> budget -> allocation -> compaction in one call."""
     conf = np.asarray(conf)

@@ -287,6 +287,45 @@ dspark_status dspark_gather_verify_tokens(const int32_t *verify_idx,
                               reinterpret_cast<cudaStream_t>(stream));
 }
 
+dspark_status dspark_greedy_verify(
+    const void *target_logits, int32_t logits_dtype, int64_t row_stride,
+    int32_t vocab, const int32_t *draft_tokens, const int32_t *draft_len,
+    const int32_t *cu_len, const uint8_t *sampling_mask, int32_t N, int32_t K,
+    int32_t *target_argmax, int32_t *accepted, int32_t *bonus,
+    void *workspace, size_t workspace_bytes, dspark_stream_t stream) {
+  dspark_status s = check_select_dims(N, K);
+  if (s != DSPARK_OK) return s;
+  if (!target_logits || !draft_tokens || !draft_len || !cu_len ||
+      !target_argmax || !accepted || !bonus)
+    return DSPARK_ERR_INVALID_ARG;
+  if (logits_dtype != DSPARK_BF16 && logits_dtype != DSPARK_F32)
+    return DSPARK_ERR_INVALID_ARG;
+  const int vec = logits_dtype == DSPARK_BF16 ? 8 : 4;
+  if (vocab <= 0 || vocab % vec != 0) return DSPARK_ERR_UNSUPPORTED;
+  if (row_stride < vocab || row_stride % vec != 0 || !aligned(target_logits, 16))
+    return DSPARK_ERR_INVALID_ARG;
+  if ((s = check_ws(workspace, workspace_bytes, kSelectWorkspaceBytes)) !=
+      DSPARK_OK)
+    return s;
+  VerifyArgs a;
+  a.target_logits = target_logits;
+  a.logits_dtype = logits_dtype;
+  a.row_stride = row_stride;
+  a.vocab = vocab;
+  a.draft = draft_tokens;
+  a.draft_len = draft_len;
+  a.cu_len = cu_len;
+  a.mask = sampling_mask;
+  a.N = N;
+  a.K = K;
+  a.target_argmax = target_argmax;
+  a.accepted = accepted;
+  a.bonus = bonus;
+  a.status = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) +
+                                          kStatusOffset);
+  return greedy_verify_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 dspark_status dspark_force_monotone(const float *cost_in, float *cost_out,
                                     int32_t cost_len, uint32_t mode,
                                     dspark_stream_t stream) {

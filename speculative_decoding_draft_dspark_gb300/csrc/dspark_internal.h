@@ -75,6 +75,23 @@ enum SelectStage : uint32_t {
   kStageCompact = 8u,   // offsets and the flattened verify list
 };
 
+struct VerifyArgs {
+  const void *target_logits;
+  int32_t logits_dtype;
+  int64_t row_stride;  // elements
+  int32_t vocab;
+  const int32_t *draft;
+  const int32_t *draft_len;
+  const int32_t *cu_len;
+  const uint8_t *mask;
+  int32_t N, K;
+  int32_t *target_argmax;
+  int32_t *accepted;
+  int32_t *bonus;
+  uint32_t *status;
+};
+dspark_status greedy_verify_launch(const VerifyArgs &a, cudaStream_t stream);
+
 dspark_status select_launch(const SelectArgs &a, uint32_t stages,
                             cudaStream_t stream);
 dspark_status gather_verify_launch(const int32_t *verify_idx,

@@ -63,6 +63,8 @@ _SIGS = {
                                   _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                   _P, _P, _SZ, _P]),
     "dspark_gather_verify_tokens": (_I32, [_P, _P, _P, _I32, _I32, _P, _P]),
+    "dspark_greedy_verify": (_I32, [_P, _I32, _I64, _I32, _P, _P, _P, _P, _I32,
+                                    _I32, _P, _P, _P, _P, _SZ, _P]),
     "dspark_force_monotone": (_I32, [_P, _P, _I32, _U32, _P]),
     "dspark_read_status": (_I32, [_P, _P, _P]),
     "dspark_clear_status": (_I32, [_P, _P]),
@@ -248,6 +250,25 @@ def dspark_gather_verify_tokens(verify_idx, B, draft_tokens, verify_tok, *,
         _ptr(verify_idx), _ptr(B), _ptr(draft_tokens), N, K, _ptr(verify_tok),
         _stream(stream))
     return _check("dspark_gather_verify_tokens", code, raise_on_error)
+
+
+def dspark_greedy_verify(target_logits, draft_tokens, draft_len, cu_len,
+                         sampling_mask, target_argmax, accepted, bonus,
+                         workspace, *, vocab=None, row_stride=None,
+                         logits_dtype=None, stream=None,
+                         raise_on_error=True) -> int:
+    import torch
+    if logits_dtype is None:
+        logits_dtype = BF16 if target_logits.dtype == torch.bfloat16 else F32
+    vocab = target_logits.shape[-1] if vocab is None else vocab
+    row_stride = target_logits.stride(0) if row_stride is None else row_stride
+    N, K = draft_tokens.shape
+    code = load().dspark_greedy_verify(
+        _ptr(target_logits), logits_dtype, row_stride, vocab,
+        _ptr(draft_tokens), _ptr(draft_len), _ptr(cu_len), _ptr(sampling_mask),
+        N, K, _ptr(target_argmax), _ptr(accepted), _ptr(bonus),
+        _ptr(workspace), _nbytes(workspace), _stream(stream))
+    return _check("dspark_greedy_verify", code, raise_on_error)
 
 
 def dspark_force_monotone(cost_in, cost_out, mode=COST_FORCE_MONOTONE, *,

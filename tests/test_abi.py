@@ -17,7 +17,7 @@ def lib():
 
 def test_exports_every_header_function(lib):
     names = D.header_functions()
-    assert len(names) == 15
+    assert len(names) == 16
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(D._SIGS)

@@ -212,3 +212,42 @@ def test_greedy_stop_differs_from_global_argmax_on_a_staircase():
     assert g["B"] == 1      # f(2) on the 30 us step is below f(1)
     assert a["B"] == 8      # the whole step pays for itself further on
     assert a["objective"] > g["objective"]
+
+
+def test_greedy_verify_hand_instance():
+    """Two sampling requests and one in prefill; target rows built so the
+    matches are known: request 0 accepts 2 of 3 and gets the target's third
+    token as bonus, request 2 accepts its single draft and gets the bonus
+    from its second row ("DSpark on MAX", *The kernel pass*, item 2)."""
+    vocab = 16
+    draft = np.array([[3, 5, 7], [1, 1, 1], [9, 0, 0]])
+    draft_len = np.array([3, 0, 1])
+    mask = np.array([1, 0, 1], np.uint8)
+    rows = oracle.verify_rows(draft_len, mask)
+    assert rows.tolist() == [0, 4, 4, 6]
+    tl = np.zeros((6, vocab), np.float32)
+    best = [3, 5, 8, 2, 9, 4]        # row r's argmax
+    for r, b in enumerate(best):
+        tl[r, b] = 1.0
+    tl[5, 4] = tl[5, 11] = 1.0       # tie: the lower index wins
+    r = oracle.greedy_verify(tl, "f32", draft, draft_len, mask)
+    assert r["target_argmax"].tolist() == best
+    assert r["accepted"].tolist() == [2, -1, 1]
+    assert r["bonus"].tolist() == [8, -1, 4]
+
+
+def test_greedy_verify_accepts_everything_when_target_agrees():
+    rng = np.random.default_rng(4)
+    N, K, vocab = 5, 4, 64
+    draft = rng.integers(0, vocab, (N, K))
+    ln = rng.integers(0, K + 1, N)
+    mask = np.ones(N, np.uint8)
+    rows = oracle.verify_rows(ln, mask)
+    tl = rng.normal(size=(rows[-1], vocab)).astype(np.float32)
+    for n in range(N):
+        for j in range(ln[n]):
+            tl[rows[n] + j, draft[n, j]] = 100.0
+    r = oracle.greedy_verify(tl, "f32", draft, ln, mask)
+    assert r["accepted"].tolist() == ln.tolist()
+    for n in range(N):
+        assert r["bonus"][n] == np.argmax(tl[rows[n] + ln[n]])
