@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-graph", action="store_true",
                     help="launch eagerly instead of replaying CUDA graphs")
+    ap.add_argument("--no-verify", action="store_true",
+                    help="skip the extra greedy-verification measurement")
     ap.add_argument("--serial", action="store_true",
                     help="run the scheduler after the chain on one stream "
                          "instead of alongside it")
@@ -418,12 +420,63 @@ def run_gpu(args):
     }
     if rank == 0:
         result["e2e"] = run_e2e(st, cfg, stream, args.e2e_steps)
+        if not args.no_verify:
+            result["next_greedy_verify"] = run_greedy_verify(st, cfg, stream)
         if world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(cfg)
         print(json.dumps(result), flush=True)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def run_greedy_verify(st, cfg, stream, iters=100):
+    """Downstream of the step (not part of the metric): greedy verification
+    of this step's verify list against synthetic target logits (one row per
+    verified draft token plus one bonus row per sampling request), timed
+    with CUDA events; reports the streaming argmax's HBM roofline."""
+    import numpy as np
+    import torch
+    import workloads
+    D = st.D
+    ln = st.ln.cpu().numpy()
+    mask = st.sel["mask"]
+    R = int(ln.sum() + mask.sum())
+    rng = np.random.default_rng(cfg.seed + 77)
+    x = rng.standard_normal((R, cfg.vocab), dtype=np.float32) * np.float32(2.0)
+    tl = torch.from_numpy(workloads.f32_to_bf16_bits(x).view(np.int16)).to(
+        st.logits.device).view(torch.bfloat16)
+    del x
+    N, K = cfg.N, cfg.K
+    tgt = torch.zeros(N * (K + 1), dtype=torch.int32, device=tl.device)
+    acc = torch.zeros(N, dtype=torch.int32, device=tl.device)
+    bon = torch.zeros(N, dtype=torch.int32, device=tl.device)
+    ws = D.new_workspace(256, tl.device)
+
+    def one():
+        D.dspark_greedy_verify(tl, st.draft, st.ln, st.cu, st.mask, tgt, acc,
+                               bon, ws)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one()
+    stream.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        s.record(stream)
+        for _ in range(iters):
+            one()
+        e.record(stream)
+    stream.synchronize()
+    us = s.elapsed_time(e) * 1e3 / iters
+    hbm = measured_peaks()[0]
+    nbytes = R * cfg.vocab * 2
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us": round(us, 2), "rows": R, "bytes": nbytes,
+            "achieved_GBs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4),
+            "note": "dspark_greedy_verify (row argmax + acceptance), not part "
+                    "of the step metric"}
 
 
 def run_e2e(st, cfg, stream, steps):
