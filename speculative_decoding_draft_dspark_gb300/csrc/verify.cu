@@ -7,13 +7,17 @@
 //
 // row_argmax_kernel: the target's best token of every verify row (one row
 // per verified draft token plus the bonus position of each sampling
-// request).  A persistent grid streams rows through an 8-stage ring of
-// 16 KB shared-memory buffers filled by 1-D bulk copies (one producer
-// thread); 16 consumer warps take the NaN-propagating maximum of eight bf16
-// values per 16-byte load with packed bf16x2 max instructions and look for
-// the first index only when that maximum beats the running best (the
-// "eight values per load" and "1,024 threads per row" lessons of the same
-// section).  Ties keep the lowest index; the first NaN wins.
+// request).  A persistent grid, two CTAs per SM, streams rows through a
+// 6-stage ring of 16 KB shared-memory buffers per CTA filled by 1-D bulk
+// copies (one producer thread).  Each thread of the 16 consumer warps takes
+// two 16-byte vectors of a stage, reduces their values with packed
+// NaN-propagating bf16x2 max instructions and keeps only its running maximum
+// and the first stage that held it: no index work per element (the "eight
+// values per load" lesson of the same section, carried further).  At the end
+// of a row the lanes holding their warp's maximum re-read their 32 bytes of
+// that stage, which the row streamed moments earlier, to find its first
+// position.  Ties keep the lowest
+// index; the first NaN wins.
 //
 // greedy_accept_kernel: per sampling request, the leading draft tokens that
 // equal the target's best tokens, and the target's token after them (bonus).
@@ -29,7 +33,10 @@ namespace dspark {
 constexpr int VA_CONSUMER_WARPS = 16;
 constexpr int VA_THREADS = (VA_CONSUMER_WARPS + 1) * 32;
 constexpr int VA_CHUNK = 16384;  // bytes per stage
-constexpr int VA_STAGES = 8;
+constexpr int VA_STAGES = 6;
+constexpr int VA_CTAS_PER_SM = 2;  // two rows in flight per SM
+// 16-byte vectors per consumer thread in a full stage
+constexpr int VA_VPT = VA_CHUNK / 16 / (VA_CONSUMER_WARPS * 32);
 constexpr int VA_RING = VA_STAGES + 1;  // row-partial buffers in flight
 constexpr int VA_SMEM_BYTES =
     VA_STAGES * VA_CHUNK + 2 * VA_STAGES * 8 +
@@ -66,7 +73,7 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 template <int LDT>
-__global__ void __launch_bounds__(VA_THREADS, 1)
+__global__ void __launch_bounds__(VA_THREADS, VA_CTAS_PER_SM)
     row_argmax_kernel(const RowArgmaxParams p) {
   extern __shared__ __align__(128) uint8_t vsm[];
   uint8_t *stages = vsm;
@@ -143,86 +150,106 @@ __global__ void __launch_bounds__(VA_THREADS, 1)
     __syncwarp();
   } else {
     // --------------------------------------------------------- consumers
-    const int ct = tid;  // 0 .. 16*32-1
+    const int ct = tid;  // 0 .. 8*32-1
     constexpr int NCT = VA_CONSUMER_WARPS * 32;
+    // fill for vectors past the end of a ragged stage: -inf never beats a
+    // real value and the index search below skips those vectors
+    constexpr uint32_t NEG_INF_WORD = LDT == DSPARK_BF16 ? 0xFF80FF80u : 0xFF800000u;
     int it = 0, rl = 0;
     bool ok = true;
     for (int r = blockIdx.x; r < R && ok; r += gridDim.x, ++rl) {
+      // per thread: its largest value in the row and the first stage holding
+      // it; where in that stage is found once, at the end of the row
       float best = -INFINITY;
-      int best_idx = INT_MAX;
-      bool have = false;
+      int best_c = -1;
       for (int c = 0; c < chunks; ++c, ++it) {
         const int s = it % VA_STAGES;
         const uint32_t ph = (it / VA_STAGES) & 1;
         ok = __all_sync(0xFFFFFFFFu, wait_bounded(&full[s], ph, abort_flag, p.status));
         if (!ok) break;
         const uint32_t off = static_cast<uint32_t>(c) * VA_CHUNK;
-        const uint32_t bytes = min(static_cast<uint32_t>(VA_CHUNK), row_bytes - off);
-        const int nvec = static_cast<int>(bytes / 16);
+        const int nvec = static_cast<int>(min(static_cast<uint32_t>(VA_CHUNK), row_bytes - off) / 16);
         const uint32_t base = smem_u32(stages + s * VA_CHUNK);
-        const int e0 = static_cast<int>(off / ESZ);
-        for (int v = ct; v < nvec; v += NCT) {
-          const uint4 w = ld_shared_v4(base + v * 16);
-          float m;
-          if constexpr (LDT == DSPARK_BF16) {
-            const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(w.x, w.y),
-                                               bf16x2_max_nan(w.z, w.w));
-            m = fmax_nan(bf16_lo(m2), bf16_hi(m2));
-          } else {
-            m = fmax_nan(fmax_nan(__uint_as_float(w.x), __uint_as_float(w.y)),
-                         fmax_nan(__uint_as_float(w.z), __uint_as_float(w.w)));
-          }
-          // only a better maximum (or a first NaN) needs its index
-          const bool better = !have || m > best || (m != m && best == best);
-          if (better) {
-            float vals[EPV];
-            if constexpr (LDT == DSPARK_BF16) {
-              const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+        uint4 w[VA_VPT];
 #pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                vals[2 * h] = bf16_lo(ww[h]);
-                vals[2 * h + 1] = bf16_hi(ww[h]);
-              }
-            } else {
-              vals[0] = __uint_as_float(w.x);
-              vals[1] = __uint_as_float(w.y);
-              vals[2] = __uint_as_float(w.z);
-              vals[3] = __uint_as_float(w.w);
-            }
-            int ie = 0;
-            if (m != m) {
-#pragma unroll
-              for (int e = EPV - 1; e >= 0; --e) ie = (vals[e] != vals[e]) ? e : ie;
-            } else {
-#pragma unroll
-              for (int e = EPV - 1; e >= 0; --e) ie = (vals[e] == m) ? e : ie;
-            }
-            best = m;
-            best_idx = e0 + v * EPV + ie;
-            have = true;
-          }
+        for (int u = 0; u < VA_VPT; ++u) {
+          const int v = ct + u * NCT;  // ascending index with u
+          w[u] = v < nvec ? ld_shared_v4(base + v * 16)
+                          : make_uint4(NEG_INF_WORD, NEG_INF_WORD, NEG_INF_WORD, NEG_INF_WORD);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+        float m;
+        if constexpr (LDT == DSPARK_BF16) {
+          uint32_t t[VA_VPT];
+#pragma unroll
+          for (int u = 0; u < VA_VPT; ++u)
+            t[u] = bf16x2_max_nan(bf16x2_max_nan(w[u].x, w[u].y), bf16x2_max_nan(w[u].z, w[u].w));
+#pragma unroll
+          for (int h = VA_VPT / 2; h >= 1; h >>= 1)
+#pragma unroll
+            for (int u = 0; u < h; ++u) t[u] = bf16x2_max_nan(t[u], t[u + h]);
+          m = fmax_nan(bf16_lo(t[0]), bf16_hi(t[0]));
+        } else {
+          float t[VA_VPT];
+#pragma unroll
+          for (int u = 0; u < VA_VPT; ++u)
+            t[u] = fmax_nan(fmax_nan(__uint_as_float(w[u].x), __uint_as_float(w[u].y)),
+                            fmax_nan(__uint_as_float(w[u].z), __uint_as_float(w[u].w)));
+#pragma unroll
+          for (int h = VA_VPT / 2; h >= 1; h >>= 1)
+#pragma unroll
+            for (int u = 0; u < h; ++u) t[u] = fmax_nan(t[u], t[u + h]);
+          m = t[0];
+        }
+        // strictly larger (or the first NaN): earlier stages keep ties
+        const bool better = ct < nvec && (best_c < 0 || m > best || (m != m && best == best));
+        best = better ? m : best;
+        best_c = better ? c : best_c;
       }
       if (!ok) break;
-      // warp reduction of (key, index): larger key, then smaller index
-      uint32_t key = have ? f32_key(best) : 0u;
-      int idx = best_idx;
+      // warp maximum; the lanes holding it find their first position in
+      // their stage by re-reading those bytes (just streamed, so from L2)
+      const uint32_t key = best_c >= 0 ? f32_key(best) : 0u;
+      const uint32_t wkey = __reduce_max_sync(0xFFFFFFFFu, key);
+      int idx = INT_MAX;
+      if (best_c >= 0 && key == wkey) {
+        const uint32_t off = static_cast<uint32_t>(best_c) * VA_CHUNK;
+        const int nvec = static_cast<int>(min(static_cast<uint32_t>(VA_CHUNK), row_bytes - off) / 16);
+        const uint8_t *src = p.logits + static_cast<int64_t>(r) * p.row_stride_bytes + off;
+        const bool want_nan = best != best;
+        for (int u = VA_VPT - 1; u >= 0; --u) {
+          const int v = ct + u * NCT;
+          if (v >= nvec) continue;
+          const uint4 w = __ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(v) * 16));
+          float vals[EPV];
+          if constexpr (LDT == DSPARK_BF16) {
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const uint32_t k2 = __shfl_down_sync(0xFFFFFFFFu, key, o);
-        const int i2 = __shfl_down_sync(0xFFFFFFFFu, idx, o);
-        if (k2 > key || (k2 == key && i2 < idx)) {
-          key = k2;
-          idx = i2;
+            for (int h = 0; h < 4; ++h) {
+              vals[2 * h] = bf16_lo(ww[h]);
+              vals[2 * h + 1] = bf16_hi(ww[h]);
+            }
+          } else {
+            vals[0] = __uint_as_float(w.x);
+            vals[1] = __uint_as_float(w.y);
+            vals[2] = __uint_as_float(w.z);
+            vals[3] = __uint_as_float(w.w);
+          }
+#pragma unroll
+          for (int e = EPV - 1; e >= 0; --e) {
+            const bool hit = want_nan ? (vals[e] != vals[e]) : (vals[e] == best);
+            idx = hit ? static_cast<int>(off / ESZ) + v * EPV + e : idx;
+          }
         }
       }
+      idx = __reduce_min_sync(0xFFFFFFFFu, idx);
+      const uint32_t key_w = wkey;
       const int b = rl % VA_RING;
       volatile unsigned long long *pb =
           reinterpret_cast<volatile unsigned long long *>(partial) + b * (VA_CONSUMER_WARPS + 1);
       if (lane == 0) {
-        pb[warp] = (static_cast<unsigned long long>(key) << 32) |
+        pb[warp] = (static_cast<unsigned long long>(key_w) << 32) |
                    static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(idx));
         __threadfence_block();
         const unsigned long long done = atomicAdd(
@@ -333,7 +360,7 @@ dspark_status greedy_verify_launch(const VerifyArgs &a, cudaStream_t stream) {
   p.out = a.target_argmax;
   p.status = a.status;
   const int rows_max = a.N * (a.K + 1);
-  const int grid = std::max(1, std::min(sms, rows_max));
+  const int grid = std::max(1, std::min(VA_CTAS_PER_SM * sms, rows_max));
   if (a.logits_dtype == DSPARK_BF16)
     row_argmax_kernel<DSPARK_BF16><<<grid, VA_THREADS, VA_SMEM_BYTES, stream>>>(p);
   else
