@@ -422,6 +422,7 @@ def run_gpu(args):
         result["e2e"] = run_e2e(st, cfg, stream, args.e2e_steps)
         if not args.no_verify:
             result["next_greedy_verify"] = run_greedy_verify(st, cfg, stream)
+            result["next_stale_select"] = run_stale_select(st, cfg, stream)
         if world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(cfg)
         print(json.dumps(result), flush=True)
@@ -477,6 +478,42 @@ def run_greedy_verify(st, cfg, stream, iters=100):
             "achieved_GBs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4),
             "note": "dspark_greedy_verify (row argmax + acceptance), not part "
                     "of the step metric"}
+
+
+def run_stale_select(st, cfg, stream, iters=200):
+    """Scheduler variant (not part of the metric): B sized from a confidence
+    buffer one step old, allocation by the current confidences, against the
+    plain fused scheduler on the same inputs; single-CTA, latency-bound."""
+    import torch
+    import workloads
+    D = st.D
+    old = torch.from_numpy(workloads.make_stale_confidences(cfg, 1)).to(st.conf.device)
+
+    def stale():
+        D.dspark_select_step_stale(old, st.conf, st.mask, st.cost, st.T, 0.0,
+                                   st.flags, st.draft, st.surv, st.srt, st.pre,
+                                   st.ne, st.ns, st.B, st.obj, st.ln, st.cu,
+                                   st.vi, st.vt, st.sws)
+
+    out = {}
+    for name, fn in (("stale_us", stale), ("plain_us", st.select)):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        stream.synchronize()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            s.record(stream)
+            for _ in range(iters):
+                fn()
+            e.record(stream)
+        stream.synchronize()
+        out[name] = round(s.elapsed_time(e) * 1e3 / iters, 2)
+    out["note"] = ("dspark_select_step_stale (two sorts in one CTA) vs "
+                   "dspark_select_step; back-to-back calls, not part of the "
+                   "step metric")
+    return out
 
 
 def run_e2e(st, cfg, stream, steps):

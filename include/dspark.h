@@ -245,6 +245,33 @@ DSPARK_API dspark_status dspark_select_step(
     int32_t *verify_tok,
     void *workspace, size_t workspace_bytes, dspark_stream_t stream);
 
+/* Stale sizing.  "Adaptive Verification in vLLM", "Scheduling the budget",
+ * last paragraph: B is sized from a double-buffered confidence array that is
+ * one step old, while handing the B slots to requests uses current
+ * confidences; "How DSpark Speeds Up LLM Inference", appendix Part B: the
+ * capacity comes from confidences two steps earlier.
+ * conf_size in [N, K] fp32: the older buffer, aligned slot by slot with the
+ *           current batch (the caller keeps it); must not be NULL.
+ * conf      in [N, K] fp32: the current confidences.
+ * Every other argument is as for dspark_select_step, with the current
+ * sampling_mask and T applying to both buffers.  B, objective and prefix_sum
+ * come from conf_size (survival, order, exact prefix sums, f(b)); survival,
+ * sorted_slots, n_eligible, n_sampling, draft_len, cu_len, verify_idx and
+ * verify_tok come from conf, whose B best slots are allocated (B never
+ * exceeds the eligible slot count, which both buffers share).  Status bits
+ * from either buffer are raised.  One single-CTA launch, which sorts twice.
+ */
+DSPARK_API dspark_status dspark_select_step_stale(
+    const float *conf_size, const float *conf, const uint8_t *sampling_mask,
+    int32_t N, int32_t K, const float *cost, int32_t cost_len,
+    const int32_t *T_dev, float draft_cost, uint32_t flags,
+    const int32_t *draft_tokens, float *survival, int32_t *sorted_slots,
+    double *prefix_sum, int32_t *n_eligible, int32_t *n_sampling,
+    int32_t *B, double *objective,
+    int32_t *draft_len, int32_t *cu_len, int32_t *verify_idx,
+    int32_t *verify_tok,
+    void *workspace, size_t workspace_bytes, dspark_stream_t stream);
+
 /* Verify tokens of the compacted list: verify_tok[j] = draft_tokens[
  * verify_idx[j]] for j < *B (B and verify_idx as written by the scheduler).
  * The scheduler does not depend on the draft except for these tokens, so a

@@ -27,10 +27,20 @@ What it computes, step by step, with the passage each step follows:
   Speeds Up LLM Inference", appendix Part B): each request gets its selected
   prefix; the verify list is flattened across requests with per-request
   offsets.
+* Stale sizing (same page, *Scheduling the budget*, last paragraph: B is
+  sized from a double-buffered confidence array one step old while the
+  allocation uses current confidences; "How DSpark Speeds Up LLM Inference",
+  appendix Part B: capacity from confidences two steps earlier): the budget
+  steps run on the older buffer, the order and allocation on the current one.
+* Greedy verification ("DSpark on MAX", *The kernel pass*, item 2): a draft
+  token is accepted iff it equals the target's best token; the longest
+  accepted run is kept and the target's next token is added.
 
 Readings of points the pages leave open: exact cumulative sums (rounded
 once), first-index argmax with NaN ranked highest, slot ties broken by slot
-id, running-max forcing, b <= L-1-T, confidences clamped into [0, 1].
+id, running-max forcing, b <= L-1-T, confidences clamped into [0, 1]; for
+stale sizing the older buffer is aligned slot by slot with the current batch
+and the current sampling mask and T apply to both passes.
 
 Every function is pinned by ``tests/test_oracle_*.py`` against values and
 properties the pages and the mathematics fix (a worked instance, brute force
@@ -320,3 +330,31 @@ def select_step(conf, mask, cost, T, draft_cost=0.0, flags=0, draft=None) -> dic
                 f=bud["f"], draft_len=ln, cu_len=cp["cu_len"],
                 verify_idx=cp["verify_idx"], verify_tok=cp["verify_tok"],
                 cost_used=cost_used, status=st | bud["status"])
+
+
+def select_step_stale(conf_size, conf, mask, cost, T, draft_cost=0.0, flags=0,
+                      draft=None) -> dict:
+    """Stale sizing ("Adaptive Verification in vLLM", *Scheduling the budget*,
+    last paragraph; "How DSpark Speeds Up LLM Inference", appendix Part B).
+
+    B (and the prefix sums and objective behind it) comes from ``conf_size``,
+    an older confidence buffer aligned slot by slot with the current batch;
+    the survival, the order and the allocation of those B slots come from the
+    current ``conf``.  The current mask and T serve both passes, so both have
+    the same number of eligible slots and B never exceeds it.
+    """
+    sized = select_step(conf_size, mask, cost, T, draft_cost, flags)
+    conf = np.asarray(conf)
+    N, K = conf.shape
+    mask = np.ones(N, np.uint8) if mask is None else np.asarray(mask)
+    s, st = survival(conf, mask)
+    order = order_slots(s, mask)
+    B = min(sized["B"], len(order))
+    ln = allocate(order, B, N, K)
+    cp = compact(ln, K, draft)
+    return dict(survival=s, order=order, n_sampling=sized["n_sampling"],
+                n_eligible=len(order), prefix=sized["prefix"], B=B,
+                objective=sized["objective"], b_max=sized["b_max"],
+                f=sized["f"], draft_len=ln, cu_len=cp["cu_len"],
+                verify_idx=cp["verify_idx"], verify_tok=cp["verify_tok"],
+                cost_used=sized["cost_used"], status=st | sized["status"])

@@ -48,6 +48,57 @@ static SelectArgs empty_select_args(void *ws) {
   return a;
 }
 
+static bool flags_ok(uint32_t flags) {
+  return (flags & ~(DSPARK_COST_FORCE_MONOTONE | DSPARK_COST_FORCE_SUFFIX_MIN |
+                    DSPARK_BUDGET_GREEDY_STOP)) == 0;
+}
+
+static dspark_status select_step_common(
+    const float *conf_size, const float *conf, const uint8_t *sampling_mask,
+    int32_t N, int32_t K, const float *cost, int32_t cost_len,
+    const int32_t *T_dev, float draft_cost, uint32_t flags,
+    const int32_t *draft_tokens, float *survival, int32_t *sorted_slots,
+    double *prefix_sum, int32_t *n_eligible, int32_t *n_sampling, int32_t *B,
+    double *objective, int32_t *draft_len, int32_t *cu_len,
+    int32_t *verify_idx, int32_t *verify_tok, void *workspace,
+    size_t workspace_bytes, dspark_stream_t stream) {
+  dspark_status s = check_select_dims(N, K);
+  if (s != DSPARK_OK) return s;
+  if (!conf || !cost || !T_dev || !B || !draft_len || !cu_len || !verify_idx)
+    return DSPARK_ERR_INVALID_ARG;
+  if (cost_len <= 0 || cost_len > (1 << 30)) return DSPARK_ERR_INVALID_ARG;
+  if (!flags_ok(flags)) return DSPARK_ERR_INVALID_ARG;
+  if ((s = check_ws(workspace, workspace_bytes, kSelectWorkspaceBytes)) !=
+      DSPARK_OK)
+    return s;
+  SelectArgs a = empty_select_args(workspace);
+  a.conf = conf;
+  a.conf_size = conf_size;
+  a.mask = sampling_mask;
+  a.N = N;
+  a.K = K;
+  a.cost = cost;
+  a.L = cost_len;
+  a.T_dev = T_dev;
+  a.draft_cost = draft_cost;
+  a.flags = flags;
+  a.draft = draft_tokens;
+  a.survival = survival;
+  a.sorted_slots = sorted_slots;
+  a.prefix_sum = prefix_sum;
+  a.n_eligible = n_eligible;
+  a.n_sampling = n_sampling;
+  a.B = B;
+  a.objective = objective;
+  a.draft_len = draft_len;
+  a.cu_len = cu_len;
+  a.verify_idx = verify_idx;
+  a.verify_tok = verify_tok;
+  return select_launch(a,
+                       kStageSurvival | kStageBudget | kStageAllocate |
+                           kStageCompact,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
 }  // namespace dspark
 
 using namespace dspark;
@@ -149,11 +200,6 @@ dspark_status dspark_survival_topb(const float *conf,
   return select_launch(a, kStageSurvival, reinterpret_cast<cudaStream_t>(stream));
 }
 
-static bool flags_ok(uint32_t flags) {
-  return (flags & ~(DSPARK_COST_FORCE_MONOTONE | DSPARK_COST_FORCE_SUFFIX_MIN |
-                    DSPARK_BUDGET_GREEDY_STOP)) == 0;
-}
-
 dspark_status dspark_choose_budget(const double *prefix_sum,
                                    const int32_t *n_eligible,
                                    const int32_t *n_sampling, const float *cost,
@@ -237,41 +283,28 @@ dspark_status dspark_select_step(
     int32_t *draft_len, int32_t *cu_len, int32_t *verify_idx,
     int32_t *verify_tok, void *workspace, size_t workspace_bytes,
     dspark_stream_t stream) {
-  dspark_status s = check_select_dims(N, K);
-  if (s != DSPARK_OK) return s;
-  if (!conf || !cost || !T_dev || !B || !draft_len || !cu_len || !verify_idx)
-    return DSPARK_ERR_INVALID_ARG;
-  if (cost_len <= 0 || cost_len > (1 << 30)) return DSPARK_ERR_INVALID_ARG;
-  if (!flags_ok(flags)) return DSPARK_ERR_INVALID_ARG;
-  if ((s = check_ws(workspace, workspace_bytes, kSelectWorkspaceBytes)) !=
-      DSPARK_OK)
-    return s;
-  SelectArgs a = empty_select_args(workspace);
-  a.conf = conf;
-  a.mask = sampling_mask;
-  a.N = N;
-  a.K = K;
-  a.cost = cost;
-  a.L = cost_len;
-  a.T_dev = T_dev;
-  a.draft_cost = draft_cost;
-  a.flags = flags;
-  a.draft = draft_tokens;
-  a.survival = survival;
-  a.sorted_slots = sorted_slots;
-  a.prefix_sum = prefix_sum;
-  a.n_eligible = n_eligible;
-  a.n_sampling = n_sampling;
-  a.B = B;
-  a.objective = objective;
-  a.draft_len = draft_len;
-  a.cu_len = cu_len;
-  a.verify_idx = verify_idx;
-  a.verify_tok = verify_tok;
-  return select_launch(a,
-                       kStageSurvival | kStageBudget | kStageAllocate |
-                           kStageCompact,
-                       reinterpret_cast<cudaStream_t>(stream));
+  return dspark::select_step_common(
+      nullptr, conf, sampling_mask, N, K, cost, cost_len, T_dev, draft_cost,
+      flags, draft_tokens, survival, sorted_slots, prefix_sum, n_eligible,
+      n_sampling, B, objective, draft_len, cu_len, verify_idx, verify_tok,
+      workspace, workspace_bytes, stream);
+}
+
+dspark_status dspark_select_step_stale(
+    const float *conf_size, const float *conf, const uint8_t *sampling_mask,
+    int32_t N, int32_t K, const float *cost, int32_t cost_len,
+    const int32_t *T_dev, float draft_cost, uint32_t flags,
+    const int32_t *draft_tokens, float *survival, int32_t *sorted_slots,
+    double *prefix_sum, int32_t *n_eligible, int32_t *n_sampling, int32_t *B,
+    double *objective, int32_t *draft_len, int32_t *cu_len,
+    int32_t *verify_idx, int32_t *verify_tok, void *workspace,
+    size_t workspace_bytes, dspark_stream_t stream) {
+  if (!conf_size) return DSPARK_ERR_INVALID_ARG;
+  return dspark::select_step_common(
+      conf_size, conf, sampling_mask, N, K, cost, cost_len, T_dev, draft_cost,
+      flags, draft_tokens, survival, sorted_slots, prefix_sum, n_eligible,
+      n_sampling, B, objective, draft_len, cu_len, verify_idx, verify_tok,
+      workspace, workspace_bytes, stream);
 }
 
 dspark_status dspark_gather_verify_tokens(const int32_t *verify_idx,

@@ -38,6 +38,9 @@ dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream);
 
 struct SelectArgs {
   const float *conf;
+  // optional older confidence buffer: when set (fused call only), the budget
+  // is sized from it and the order and allocation use `conf`
+  const float *conf_size;
   const uint8_t *mask;
   int32_t N, K;
   const float *cost;

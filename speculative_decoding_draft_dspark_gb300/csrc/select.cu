@@ -479,6 +479,58 @@ __device__ void block_bitonic(unsigned long long *keys, uint16_t *sidx,
 // ------------------------------------------------------------------------
 constexpr int kMaxChunk = (kMaxSlots + 1 + SEL_THREADS - 1) / SEL_THREADS + 1;
 
+// Survival products of `conf` (fp64, left to right, clamped), sort keys
+// (bits(s) + 1, 0 for non-sampling requests) and the bitonic order.  With
+// `outputs`, writes survival, sorted_slots, n_eligible and n_sampling.
+template <int E>
+__device__ void survival_order(const SelectArgs &a, const float *conf,
+                               const bool outputs, unsigned long long *keys,
+                               uint16_t *sidx, const int P2, int *sh_int,
+                               int &n_s, uint32_t &st) {
+  const int tid = threadIdx.x;
+  const int NT = blockDim.x;
+  const int N = a.N, K = a.K, NK = N * K;
+  int my_ns = 0;
+  for (int n = tid; n < N; n += NT) {
+    const bool samp = a.mask == nullptr || a.mask[n] != 0;
+    my_ns += samp ? 1 : 0;
+    double prod = 1.0;
+    for (int k = 0; k < K; ++k) {
+      float c = conf[static_cast<size_t>(n) * K + k];
+      if (!(c >= 0.0f && c <= 1.0f)) {
+        st |= DSPARK_DEV_CONF_OOR;
+        c = (c > 1.0f) ? 1.0f : 0.0f;  // NaN and negatives -> 0
+      }
+      if (c == 0.0f) c = 0.0f;  // -0 -> +0: sort keys are bit patterns
+      prod = __dmul_rn(prod, static_cast<double>(c));
+      if (outputs && a.survival)
+        a.survival[static_cast<size_t>(n) * K + k] =
+            samp ? __double2float_rn(prod) : 0.0f;
+      keys[n * K + k] =
+          samp ? static_cast<unsigned long long>(__double_as_longlong(prod)) + 1ull
+               : 0ull;
+      sidx[n * K + k] = static_cast<uint16_t>(n * K + k);
+    }
+  }
+  for (int i = NK + tid; i < P2; i += NT) {
+    keys[i] = 0ull;
+    sidx[i] = 0xFFFFu;
+  }
+  n_s = block_reduce(my_ns, OpAddInt(), 0, sh_int);
+  const int S = n_s * K;
+
+  __syncthreads();
+  block_bitonic<E>(keys, sidx, P2);
+  if (outputs) {
+    if (a.sorted_slots)
+      for (int j = tid; j < S; j += NT) a.sorted_slots[j] = sidx[j];
+    if (tid == 0) {
+      if (a.n_eligible) *a.n_eligible = S;
+      if (a.n_sampling) *a.n_sampling = n_s;
+    }
+  }
+}
+
 template <int E>
 __global__ void __launch_bounds__(SEL_THREADS, 1)
     select_kernel(const SelectArgs a, const uint32_t stages, const int P2) {
@@ -503,44 +555,14 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   uint32_t st = 0;
 
   // ---------------------------------------------------- survival + order
+  // Stale sizing: the budget comes from a.conf_size, then survival and order
+  // are rebuilt from a.conf for the allocation.
+  const bool stale = a.conf_size != nullptr && (stages & kStageSurvival) &&
+                     (stages & kStageBudget) && (stages & kStageAllocate);
   if (stages & kStageSurvival) {
-    int my_ns = 0;
-    for (int n = tid; n < N; n += NT) {
-      const bool samp = a.mask == nullptr || a.mask[n] != 0;
-      my_ns += samp ? 1 : 0;
-      double prod = 1.0;
-      for (int k = 0; k < K; ++k) {
-        float c = a.conf[static_cast<size_t>(n) * K + k];
-        if (!(c >= 0.0f && c <= 1.0f)) {
-          st |= DSPARK_DEV_CONF_OOR;
-          c = (c > 1.0f) ? 1.0f : 0.0f;  // NaN and negatives -> 0
-        }
-        if (c == 0.0f) c = 0.0f;  // -0 -> +0: sort keys are bit patterns
-        prod = __dmul_rn(prod, static_cast<double>(c));
-        if (a.survival)
-          a.survival[static_cast<size_t>(n) * K + k] =
-              samp ? __double2float_rn(prod) : 0.0f;
-        keys[n * K + k] =
-            samp ? static_cast<unsigned long long>(__double_as_longlong(prod)) + 1ull
-                 : 0ull;
-        sidx[n * K + k] = static_cast<uint16_t>(n * K + k);
-      }
-    }
-    for (int i = NK + tid; i < P2; i += NT) {
-      keys[i] = 0ull;
-      sidx[i] = 0xFFFFu;
-    }
-    n_s = block_reduce(my_ns, OpAddInt(), 0, sh_int);
+    survival_order<E>(a, stale ? a.conf_size : a.conf, !stale, keys, sidx, P2,
+                      sh_int, n_s, st);
     S = n_s * K;
-
-    __syncthreads();
-    block_bitonic<E>(keys, sidx, P2);
-    if (a.sorted_slots)
-      for (int j = tid; j < S; j += NT) a.sorted_slots[j] = sidx[j];
-    if (tid == 0) {
-      if (a.n_eligible) *a.n_eligible = S;
-      if (a.n_sampling) *a.n_sampling = n_s;
-    }
 
     // exact prefix sums of the sorted survivals
     int e_max = 1;
@@ -699,6 +721,16 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
       int B = *a.B_in;
       sh_B = B < 0 ? 0 : (B > NK ? NK : B);
     }
+    __syncthreads();
+  }
+
+  if (stale) {
+    // the budget pass is done with keys (its prefix sums were written over
+    // them): order the current confidences for the allocation
+    __syncthreads();
+    int n_s2 = 0;
+    survival_order<E>(a, a.conf, true, keys, sidx, P2, sh_int, n_s2, st);
+    if (tid == 0) sh_B = min(sh_B, n_s2 * K);
     __syncthreads();
   }
 

@@ -62,6 +62,9 @@ _SIGS = {
     "dspark_select_step": (_I32, [_P, _P, _I32, _I32, _P, _I32, _P, _F, _U32,
                                   _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                   _P, _P, _SZ, _P]),
+    "dspark_select_step_stale": (_I32, [_P, _P, _P, _I32, _I32, _P, _I32, _P,
+                                        _F, _U32, _P, _P, _P, _P, _P, _P, _P,
+                                        _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "dspark_gather_verify_tokens": (_I32, [_P, _P, _P, _I32, _I32, _P, _P]),
     "dspark_greedy_verify": (_I32, [_P, _I32, _I64, _I32, _P, _P, _P, _P, _I32,
                                     _I32, _P, _P, _P, _P, _SZ, _P]),
@@ -241,6 +244,25 @@ def dspark_select_step(conf, sampling_mask, cost, T_dev, draft_cost, flags,
         _ptr(cu_len), _ptr(verify_idx), _ptr(verify_tok), _ptr(workspace),
         _nbytes(workspace), _stream(stream))
     return _check("dspark_select_step", code, raise_on_error)
+
+
+def dspark_select_step_stale(conf_size, conf, sampling_mask, cost, T_dev,
+                             draft_cost, flags, draft_tokens, survival,
+                             sorted_slots, prefix_sum, n_eligible, n_sampling,
+                             B, objective, draft_len, cu_len, verify_idx,
+                             verify_tok, workspace, *, stream=None,
+                             raise_on_error=True) -> int:
+    N, K = conf.shape
+    if tuple(conf_size.shape) != (N, K):
+        raise ValueError("conf_size and conf must have the same [N, K] shape")
+    code = load().dspark_select_step_stale(
+        _ptr(conf_size), _ptr(conf), _ptr(sampling_mask), N, K, _ptr(cost),
+        cost.numel(), _ptr(T_dev), float(draft_cost), int(flags),
+        _ptr(draft_tokens), _ptr(survival), _ptr(sorted_slots),
+        _ptr(prefix_sum), _ptr(n_eligible), _ptr(n_sampling), _ptr(B),
+        _ptr(objective), _ptr(draft_len), _ptr(cu_len), _ptr(verify_idx),
+        _ptr(verify_tok), _ptr(workspace), _nbytes(workspace), _stream(stream))
+    return _check("dspark_select_step_stale", code, raise_on_error)
 
 
 def dspark_gather_verify_tokens(verify_idx, B, draft_tokens, verify_tok, *,

@@ -133,9 +133,10 @@ def _score_ok(got, want):
 
 # ----------------------------------------------------------- scheduler
 def run_select(conf, mask, cost, T, draft_cost=0.0, flags=0, draft=None,
-               fused=True):
-    """Runs the scheduler through the fused call or the four separate calls;
-    returns numpy outputs and the status word."""
+               fused=True, conf_size=None):
+    """Runs the scheduler through the fused call or the four separate calls
+    (with ``conf_size``: stale sizing, fused or composed from the separate
+    calls); returns numpy outputs and the status word."""
     N, K = conf.shape
     d_conf = up(np.asarray(conf, np.float32))
     d_mask = None if mask is None else up(np.asarray(mask, np.uint8))
@@ -151,7 +152,26 @@ def run_select(conf, mask, cost, T, draft_cost=0.0, flags=0, draft=None,
     vi = torch.full((N * K,), -1, dtype=torch.int32, device=DEV)
     vt = torch.full((N * K,), -1, dtype=torch.int32, device=DEV)
     ws = D.new_workspace(D.dspark_select_workspace_size(N, K, len(cost)), DEV)
-    if fused:
+    if conf_size is not None and fused:
+        D.dspark_select_step_stale(up(np.asarray(conf_size, np.float32)), d_conf,
+                                   d_mask, d_cost, d_T, draft_cost, flags,
+                                   d_draft, surv, srt, pre, ne, ns, B, obj, ln,
+                                   cu, vi, vt if d_draft is not None else None,
+                                   ws)
+    elif conf_size is not None:
+        # size from the old buffer, then order the current one and allocate
+        s_old = torch.zeros(N, K, dtype=torch.float32, device=DEV)
+        srt_old = torch.full((N * K,), -1, dtype=torch.int32, device=DEV)
+        pre_cur = torch.full((N * K + 1,), -1.0, dtype=torch.float64, device=DEV)
+        D.dspark_survival_topb(up(np.asarray(conf_size, np.float32)), d_mask,
+                               s_old, srt_old, pre, ne, ns, ws)
+        D.dspark_choose_budget(pre, ne, ns, d_cost, d_T, draft_cost, flags, B,
+                               obj, ws)
+        D.dspark_survival_topb(d_conf, d_mask, surv, srt, pre_cur, ne, ns, ws)
+        D.dspark_allocate_prefix(srt, B, N, K, ln, ws)
+        D.dspark_compact_verify(ln, d_draft, N, K, cu, vi,
+                                vt if d_draft is not None else None, ws)
+    elif fused:
         D.dspark_select_step(d_conf, d_mask, d_cost, d_T, draft_cost, flags,
                              d_draft, surv, srt, pre, ne, ns, B, obj, ln, cu,
                              vi, vt if d_draft is not None else None, ws)
@@ -173,9 +193,14 @@ def run_select(conf, mask, cost, T, draft_cost=0.0, flags=0, draft=None,
     return out
 
 
-def check_select(got, conf, mask, cost, T, draft_cost=0.0, flags=0, draft=None):
+def check_select(got, conf, mask, cost, T, draft_cost=0.0, flags=0, draft=None,
+                 conf_size=None):
     N, K = np.asarray(conf).shape
-    r = oracle.select_step(conf, mask, cost, T, draft_cost, flags, draft)
+    if conf_size is None:
+        r = oracle.select_step(conf, mask, cost, T, draft_cost, flags, draft)
+    else:
+        r = oracle.select_step_stale(conf_size, conf, mask, cost, T, draft_cost,
+                                     flags, draft)
     S = r["n_eligible"]
     # survival: fp64 product rounded once to fp32 on both sides
     np.testing.assert_array_equal(got["survival"], r["survival"].astype(np.float32))

@@ -17,7 +17,7 @@ def lib():
 
 def test_exports_every_header_function(lib):
     names = D.header_functions()
-    assert len(names) == 16
+    assert len(names) == 17
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(D._SIGS)
@@ -91,6 +91,25 @@ def test_select_validation(lib):
     assert lib.dspark_force_monotone(None, FAKE, 64, 1, None) == D.ERR_INVALID_ARG
     assert lib.dspark_read_status(None, ctypes.byref(ctypes.c_uint32()), None) \
         == D.ERR_INVALID_ARG
+
+
+def test_select_stale_validation(lib):
+    f = lib.dspark_select_step_stale
+    ok = dict(conf_size=FAKE, conf=FAKE, mask=None, N=4, K=7, cost=FAKE, L=64,
+              T=FAKE, dc=0.0, flags=0, draft=None, surv=None, srt=None,
+              pre=None, ne=None, ns=None, B=FAKE, obj=None, ln=FAKE, cu=FAKE,
+              vi=FAKE, vt=None, ws=FAKE * 2, wsb=256, stream=None)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(*a.values())
+
+    assert call(conf_size=None) == D.ERR_INVALID_ARG
+    assert call(conf=None) == D.ERR_INVALID_ARG
+    assert call(K=40) == D.ERR_UNSUPPORTED
+    assert call(flags=64) == D.ERR_INVALID_ARG
+    assert call(wsb=16) == D.ERR_WORKSPACE
 
 
 def test_product_path_never_touches_the_oracle():

@@ -77,3 +77,36 @@ def test_bruteforce_topb_and_budget(name, conf, cost, T):
     assert int(np.argmax(f)) == r["B"], name
     # 4) and allocation follows from the chosen top-B set
     assert r["draft_len"].sum() == r["B"]
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_bruteforce_stale_sizing(seed):
+    """Stale sizing ("Adaptive Verification in vLLM", *Scheduling the budget*,
+    last paragraph): B is the best budget for the old survivals (every subset
+    enumerated), and the allocated set is a best subset of that size for the
+    current survivals."""
+    rng = np.random.default_rng(500 + seed)
+    N, K, T = 3, 6, 2
+    old = rng.uniform(0.05, 1.0, size=(N, K)).astype(np.float32)
+    cur = rng.uniform(0.05, 1.0, size=(N, K)).astype(np.float32)
+    n = np.arange(48)
+    cost = (10 + 0.8 * n + np.where(n > 9, 6.0, 0.0)).astype(np.float32)
+    mask = np.ones(N, np.uint8)
+    r = oracle.select_step_stale(old, cur, mask, cost, T)
+    s_old = np.cumprod(old.astype(np.float64), axis=1).reshape(-1)
+    s_cur = np.cumprod(cur.astype(np.float64), axis=1).reshape(-1)
+    sums_o, cnt = _all_subset_sums(s_old)
+    sums_c, _ = _all_subset_sums(s_cur)
+    S = N * K
+    best_o = np.array([sums_o[cnt == b].max() for b in range(S + 1)])
+    bmax = min(S, len(cost) - 1 - T)
+    f = [(N + best_o[b]) / float(cost[T + b]) for b in range(bmax + 1)]
+    assert int(np.argmax(f)) == r["B"]
+    sel = 0
+    for nn in range(N):
+        for k in range(int(r["draft_len"][nn])):
+            sel |= 1 << (nn * K + k)
+    assert bin(sel).count("1") == r["B"]
+    best_c = sums_c[cnt == r["B"]].max()
+    assert sums_c[sel] >= best_c * (1 - 1e-13)
+    assert _prefix_closed(sel, N, K)

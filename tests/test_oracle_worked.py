@@ -91,3 +91,26 @@ def test_table_edges():
     # b_max clipped by the table, not by the slots
     r = oracle.select_step(d["conf"], d["mask"], d["cost"], L - 5)
     assert r["b_max"] == 4 and r["B"] <= 4
+
+
+def test_w3_stale_sizing():
+    """B from the old buffer, allocation by the current order (W3)."""
+    g = _load("w3_stale_sizing.json")
+    conf_size = np.array(g["conf_size"], np.float32)
+    conf = np.array(g["conf"], np.float32)
+    mask = np.array(g["mask"], np.uint8)
+    cost = np.array(g["cost"], np.float32)
+    r = oracle.select_step_stale(conf_size, conf, mask, cost, g["T"])
+    e = g["expected"]
+    assert r["B"] == e["B"]
+    np.testing.assert_array_equal(r["f"], np.array(e["f"]))
+    assert r["order"].tolist() == e["order"]
+    assert r["draft_len"].tolist() == e["draft_len"]
+    assert r["cu_len"].tolist() == e["cu_len"]
+    assert r["verify_idx"].tolist() == e["verify_idx"]
+    # the two wrong readings the instance separates
+    cur = oracle.select_step(conf, mask, cost, g["T"])
+    assert cur["B"] == g["if_sized_from_current"]["B"]
+    assert cur["draft_len"].tolist() == g["if_sized_from_current"]["draft_len"]
+    old = oracle.select_step(conf_size, mask, cost, g["T"])
+    assert old["draft_len"].tolist() == g["if_allocated_by_old_order"]["draft_len"]

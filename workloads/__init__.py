@@ -232,6 +232,15 @@ def make_select_inputs(cfg: Config) -> dict:
                 draft_cost=np.float32(cfg.draft_cost))
 
 
+def make_stale_confidences(cfg: Config, steps_back: int = 1) -> np.ndarray:
+    """Confidences [N,K] f32 the head gave ``steps_back`` steps earlier: the
+    same recipe as make_select_inputs, drawn from a seed of its own (the
+    mask, cost table and T of the current step are unchanged)."""
+    import dataclasses
+    old = dataclasses.replace(cfg, seed=cfg.seed + 7919 * int(steps_back))
+    return make_select_inputs(old)["conf"]
+
+
 # --------------------------------------------------------------------------
 # chain inputs: U, V (with planted duplicate rows), last token, logits rows
 # --------------------------------------------------------------------------
