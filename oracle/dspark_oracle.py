@@ -77,6 +77,57 @@ def to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# counter-based random numbers for probabilistic drafting
+# ---------------------------------------------------------------------------
+# Philox4x32-10 as defined by Salmon, Moraes, Dror and Shaw, "Parallel random
+# numbers: as easy as 1, 2, 3" (SC 2011): a 4 x 32-bit counter and a 2 x 32-bit
+# key; each of 10 rounds multiplies counter words 0 and 2 by the two round
+# multipliers, mixes the high halves with the other words and the key, and
+# bumps the key by the two Weyl constants.
+PHILOX_M0 = 0xD2511F53
+PHILOX_M1 = 0xCD9E8D57
+PHILOX_W0 = 0x9E3779B9
+PHILOX_W1 = 0xBB67AE85
+_M32 = np.uint64(0xFFFFFFFF)
+
+
+def philox4x32_10(c0, c1, c2, c3, k0, k1):
+    """Four 32-bit output words (uint64 arrays) for counters (c0..c3) and key
+    (k0, k1); inputs broadcast."""
+    c = [np.asarray(x, dtype=np.uint64) & _M32 for x in (c0, c1, c2, c3)]
+    k0 = np.asarray(k0, dtype=np.uint64) & _M32
+    k1 = np.asarray(k1, dtype=np.uint64) & _M32
+    m0, m1 = np.uint64(PHILOX_M0), np.uint64(PHILOX_M1)
+    for _ in range(10):
+        p0 = c[0] * m0  # < 2^64: exact in uint64
+        p1 = c[2] * m1
+        c = [(p1 >> np.uint64(32)) ^ c[1] ^ k0, p1 & _M32,
+             (p0 >> np.uint64(32)) ^ c[3] ^ k1, p0 & _M32]
+        k0 = (k0 + np.uint64(PHILOX_W0)) & _M32
+        k1 = (k1 + np.uint64(PHILOX_W1)) & _M32
+    return c
+
+
+def draft_uniforms(seed: int, offset: int, n: int, k: int, vocab: int) -> np.ndarray:
+    """u[v] in (0, 1) for request n, draft position k, vocabulary entry v.
+
+    Word v % 4 of Philox4x32-10 with counter (v // 4, n, k, offset) and key
+    (low, high 32 bits of seed), keeping its top 23 bits: u = (2 * (x >> 9) +
+    1) / 2^24, an odd multiple of 2^-24 that fp32 and fp64 both hold exactly.
+    """
+    v = np.arange(vocab, dtype=np.uint64)
+    words = philox4x32_10(v >> np.uint64(2), n, k, offset,
+                          seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)
+    x = np.choose((v & np.uint64(3)).astype(np.int64), words)
+    return (2.0 * (x >> np.uint64(9)).astype(np.float64) + 1.0) * 2.0 ** -24
+
+
+def gumbel_noise(seed: int, offset: int, n: int, k: int, vocab: int) -> np.ndarray:
+    """Standard Gumbel noise g = -ln(-ln u) (fp64) from draft_uniforms."""
+    return -np.log(-np.log(draft_uniforms(seed, offset, n, k, vocab)))
+
+
+# ---------------------------------------------------------------------------
 # chaining
 # ---------------------------------------------------------------------------
 def markov_bias(U64: np.ndarray, V64: np.ndarray, prev: np.ndarray) -> np.ndarray:
@@ -85,13 +136,19 @@ def markov_bias(U64: np.ndarray, V64: np.ndarray, prev: np.ndarray) -> np.ndarra
 
 
 def chain_position(logits_k64: np.ndarray, U64: np.ndarray, V64: np.ndarray,
-                   prev: np.ndarray) -> dict:
+                   prev: np.ndarray, noise: np.ndarray | None = None,
+                   tau: float = 1.0) -> dict:
     """One draft position: adjusted logits and their first-index argmax.
 
     numpy's argmax returns the first maximal index and the first NaN if a row
-    holds one, which is the tie and NaN rule of the C ABI.
+    holds one, which is the tie and NaN rule of the C ABI.  With ``noise``
+    (Gumbel values per row and token) the token is drawn from the softmax of
+    adj / tau by the Gumbel-max rule: the argmax of adj / tau + noise; the
+    score is then that perturbed value.
     """
     adj = logits_k64 + markov_bias(U64, V64, prev)
+    if noise is not None:
+        adj = adj / tau + noise
     tok = np.argmax(adj, axis=1)
     rows = np.arange(adj.shape[0])
     best = adj[rows, tok]
@@ -109,12 +166,21 @@ def chain_position(logits_k64: np.ndarray, U64: np.ndarray, V64: np.ndarray,
 
 
 def chain(logits: np.ndarray, logits_dtype: str, U: np.ndarray, V: np.ndarray,
-          last_token: np.ndarray, keep_adj: bool = False) -> dict:
+          last_token: np.ndarray, keep_adj: bool = False,
+          sample: dict | None = None, rows: np.ndarray | None = None) -> dict:
     """Chain K draft positions for every row of ``logits`` [n, K, vocab].
 
     U, V are bf16 bit patterns [vocab, rank].  Returns draft [n, K] (int64),
     the adjusted value at the chosen token, the top-2 margin and |max| per
     (row, position), and the status bits a device would raise.
+
+    ``sample`` = dict(seed, offset, tau) draws every token from the softmax
+    of the adjusted logits at temperature tau instead of taking the argmax
+    (probabilistic drafting: "Adaptive Verification in vLLM", *Appendix:
+    reproducing*, draft_sample_method "probabilistic"), by the Gumbel-max
+    rule with gumbel_noise; ``rows`` gives each row's request index n for the
+    noise counters (default 0..n-1).  Scores, margins and |max| then refer to
+    adj / tau + noise.
     """
     U64 = bf16_to_f64(U)
     V64 = bf16_to_f64(V)
@@ -130,8 +196,14 @@ def chain(logits: np.ndarray, logits_dtype: str, U: np.ndarray, V: np.ndarray,
     margin = np.zeros((n, K))
     absmax = np.zeros((n, K))
     adjs = []
+    rows = np.arange(n) if rows is None else np.asarray(rows)
     for k in range(K):
-        r = chain_position(to_f64(logits[:, k, :], logits_dtype), U64, V64, prev)
+        noise = None
+        if sample is not None:
+            noise = np.stack([gumbel_noise(int(sample["seed"]), int(sample["offset"]),
+                                           int(rr), k, vocab) for rr in rows])
+        r = chain_position(to_f64(logits[:, k, :], logits_dtype), U64, V64, prev,
+                           noise, float(sample["tau"]) if sample is not None else 1.0)
         draft[:, k] = r["tok"]
         score[:, k] = r["score"]
         margin[:, k] = r["margin"]
