@@ -423,6 +423,7 @@ def run_gpu(args):
         if not args.no_verify:
             result["next_greedy_verify"] = run_greedy_verify(st, cfg, stream)
             result["next_stale_select"] = run_stale_select(st, cfg, stream)
+            result["next_sample_chain"] = run_sample_chain(st, cfg, stream)
         if world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(cfg)
         print(json.dumps(result), flush=True)
@@ -513,6 +514,41 @@ def run_stale_select(st, cfg, stream, iters=200):
     out["note"] = ("dspark_select_step_stale (two sorts in one CTA) vs "
                    "dspark_select_step; back-to-back calls, not part of the "
                    "step metric")
+    return out
+
+
+def run_sample_chain(st, cfg, stream, iters=50):
+    """Probabilistic drafting (not part of the metric): dspark_chain_sample
+    (Gumbel-max with Philox4x32-10 noise) against dspark_chain_draft on the
+    same inputs, back-to-back launches timed with CUDA events."""
+    import torch
+    D = st.D
+
+    def sample():
+        D.dspark_chain_sample(st.logits, st.U, st.V, st.last, st.draft,
+                              st.score, st.cws, seed=0x5EED, offset=1,
+                              temperature=1.0)
+
+    out = {}
+    for name, fn in (("sample_us", sample), ("greedy_us", st.chain)):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        stream.synchronize()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            s.record(stream)
+            for _ in range(iters):
+                fn()
+            e.record(stream)
+        stream.synchronize()
+        out[name] = round(s.elapsed_time(e) * 1e3 / iters, 2)
+    elems = cfg.N * cfg.K * cfg.vocab
+    out["elements"] = elems
+    out["gelem_per_s"] = round(elems / (out["sample_us"] * 1e-6) / 1e9, 2)
+    out["note"] = ("dspark_chain_sample vs dspark_chain_draft, back-to-back "
+                   "launches; not part of the step metric")
     return out
 
 

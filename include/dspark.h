@@ -123,6 +123,35 @@ DSPARK_API dspark_status dspark_chain_draft(
     void *workspace, size_t workspace_bytes, dspark_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Probabilistic drafting.  "Adaptive Verification in vLLM", "Appendix:
+ * reproducing": the drafter runs with draft_sample_method "probabilistic",
+ * drawing each draft token from the adjusted distribution instead of taking
+ * its argmax.  Same chain, same arguments and limits as dspark_chain_draft,
+ * except that draft[n,k] is the first index of the maximum of
+ *     adj[n,k,v] / temperature + g(n, k, v),
+ * the Gumbel-max rule, so draft[n,k] ~ softmax(adj[n,k,:] / temperature)
+ * given the earlier tokens.  The noise g = -ln(-ln u) comes from a
+ * counter-based generator: x = word (v % 4) of Philox4x32-10 (Salmon et al.,
+ * SC 2011) with counter (v / 4, n, k, offset) and key (seed low 32 bits,
+ * seed high 32 bits), u = (2 (x >> 9) + 1) / 2^24; noise is fp32 (accurate
+ * logf).  The same (seed, offset) reproduces the same drafts; a caller
+ * advances offset every decoding step.
+ * temperature  > 0 and finite with a finite reciprocal, else
+ *              DSPARK_ERR_INVALID_ARG.
+ * draft_score  optional out [N, K]: the perturbed value adj/temperature + g
+ *              at draft[n,k].
+ * ------------------------------------------------------------------------ */
+DSPARK_API dspark_status dspark_chain_sample(
+    const void *logits, int32_t logits_dtype,
+    int64_t logits_stride_n, int64_t logits_stride_k,
+    const void *U, const void *V,
+    const int32_t *last_token,
+    int32_t N, int32_t K, int32_t vocab, int32_t rank,
+    uint64_t seed, uint32_t offset, float temperature,
+    int32_t *draft_tokens, float *draft_score,
+    void *workspace, size_t workspace_bytes, dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * dspark_chain_draft for callers that cannot allocate device memory.  The
  * pages have no counterpart: this is an interface convenience, not part of
  * the method.  Code running inside a CUDA graph capture, serving engines

@@ -1,6 +1,7 @@
 // C entry points of libdspark.so: host-side validation, then the launches.
 // Nothing here allocates device memory or synchronises, except
 // dspark_read_status(), which copies the status word to the host.
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -38,6 +39,51 @@ static dspark_status check_select_dims(int32_t N, int32_t K) {
 static dspark_status check_ws(const void *ws, size_t bytes, size_t need) {
   if (ws == nullptr || bytes < need || !aligned(ws, 256))
     return DSPARK_ERR_WORKSPACE;
+  return DSPARK_OK;
+}
+
+static dspark_status fill_chain_args(
+    ChainArgs &a, const void *logits, int32_t logits_dtype,
+    int64_t logits_stride_n, int64_t logits_stride_k, const void *U,
+    const void *V, const int32_t *last_token, int32_t N, int32_t K,
+    int32_t vocab, int32_t rank, int32_t *draft_tokens, float *draft_score,
+    void *workspace, size_t workspace_bytes) {
+  if (!logits || !U || !V || !last_token || !draft_tokens)
+    return DSPARK_ERR_INVALID_ARG;
+  if (logits_dtype != DSPARK_BF16 && logits_dtype != DSPARK_F32)
+    return DSPARK_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || vocab <= 0 || rank <= 0) return DSPARK_ERR_INVALID_ARG;
+  if (K > kMaxK) return DSPARK_ERR_UNSUPPORTED;
+  if (rank % 16 != 0 || rank > 256) return DSPARK_ERR_UNSUPPORTED;
+  const int esz = logits_dtype == DSPARK_BF16 ? 2 : 4;
+  const int vec = 16 / esz;  // elements per 16 bytes
+  if (vocab < vec || vocab % vec != 0) return DSPARK_ERR_UNSUPPORTED;
+  if (logits_stride_n < vocab || logits_stride_n % vec != 0)
+    return DSPARK_ERR_INVALID_ARG;
+  if (K > 1 && (logits_stride_k < vocab || logits_stride_k % vec != 0))
+    return DSPARK_ERR_INVALID_ARG;
+  if (!aligned(logits, 16) || !aligned(U, 16) || !aligned(V, 16))
+    return DSPARK_ERR_INVALID_ARG;
+  if (!aligned(last_token, 4) || !aligned(draft_tokens, 4) ||
+      (draft_score && !aligned(draft_score, 4)))
+    return DSPARK_ERR_INVALID_ARG;
+  dspark_status s =
+      check_ws(workspace, workspace_bytes, chain_workspace_bytes(N, K));
+  if (s != DSPARK_OK) return s;
+  a.logits = logits;
+  a.logits_dtype = logits_dtype;
+  a.stride_n = logits_stride_n;
+  a.stride_k = logits_stride_k;
+  a.U = U;
+  a.V = V;
+  a.last_token = last_token;
+  a.N = N;
+  a.K = K;
+  a.vocab = vocab;
+  a.rank = rank;
+  a.draft = draft_tokens;
+  a.score = draft_score;
+  a.workspace = workspace;
   return DSPARK_OK;
 }
 
@@ -127,43 +173,39 @@ dspark_status dspark_chain_draft(const void *logits, int32_t logits_dtype,
                                  float *draft_score, void *workspace,
                                  size_t workspace_bytes,
                                  dspark_stream_t stream) {
-  if (!logits || !U || !V || !last_token || !draft_tokens)
-    return DSPARK_ERR_INVALID_ARG;
-  if (logits_dtype != DSPARK_BF16 && logits_dtype != DSPARK_F32)
-    return DSPARK_ERR_INVALID_ARG;
-  if (N <= 0 || K <= 0 || vocab <= 0 || rank <= 0) return DSPARK_ERR_INVALID_ARG;
-  if (K > kMaxK) return DSPARK_ERR_UNSUPPORTED;
-  if (rank % 16 != 0 || rank > 256) return DSPARK_ERR_UNSUPPORTED;
-  const int esz = logits_dtype == DSPARK_BF16 ? 2 : 4;
-  const int vec = 16 / esz;  // elements per 16 bytes
-  if (vocab < vec || vocab % vec != 0) return DSPARK_ERR_UNSUPPORTED;
-  if (logits_stride_n < vocab || logits_stride_n % vec != 0)
-    return DSPARK_ERR_INVALID_ARG;
-  if (K > 1 && (logits_stride_k < vocab || logits_stride_k % vec != 0))
-    return DSPARK_ERR_INVALID_ARG;
-  if (!aligned(logits, 16) || !aligned(U, 16) || !aligned(V, 16))
-    return DSPARK_ERR_INVALID_ARG;
-  if (!aligned(last_token, 4) || !aligned(draft_tokens, 4) ||
-      (draft_score && !aligned(draft_score, 4)))
-    return DSPARK_ERR_INVALID_ARG;
-  dspark_status s =
-      check_ws(workspace, workspace_bytes, chain_workspace_bytes(N, K));
-  if (s != DSPARK_OK) return s;
   ChainArgs a;
-  a.logits = logits;
-  a.logits_dtype = logits_dtype;
-  a.stride_n = logits_stride_n;
-  a.stride_k = logits_stride_k;
-  a.U = U;
-  a.V = V;
-  a.last_token = last_token;
-  a.N = N;
-  a.K = K;
-  a.vocab = vocab;
-  a.rank = rank;
-  a.draft = draft_tokens;
-  a.score = draft_score;
-  a.workspace = workspace;
+  const dspark_status s = fill_chain_args(
+      a, logits, logits_dtype, logits_stride_n, logits_stride_k, U, V,
+      last_token, N, K, vocab, rank, draft_tokens, draft_score, workspace,
+      workspace_bytes);
+  if (s != DSPARK_OK) return s;
+  return chain_draft_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dspark_status dspark_chain_sample(const void *logits, int32_t logits_dtype,
+                                  int64_t logits_stride_n,
+                                  int64_t logits_stride_k, const void *U,
+                                  const void *V, const int32_t *last_token,
+                                  int32_t N, int32_t K, int32_t vocab,
+                                  int32_t rank, uint64_t seed, uint32_t offset,
+                                  float temperature, int32_t *draft_tokens,
+                                  float *draft_score, void *workspace,
+                                  size_t workspace_bytes,
+                                  dspark_stream_t stream) {
+  if (!(temperature > 0.0f) || !std::isfinite(temperature) ||
+      !std::isfinite(1.0f / temperature))
+    return DSPARK_ERR_INVALID_ARG;
+  ChainArgs a;
+  const dspark_status s = fill_chain_args(
+      a, logits, logits_dtype, logits_stride_n, logits_stride_k, U, V,
+      last_token, N, K, vocab, rank, draft_tokens, draft_score, workspace,
+      workspace_bytes);
+  if (s != DSPARK_OK) return s;
+  a.sample = 1;
+  a.seed_lo = static_cast<uint32_t>(seed);
+  a.seed_hi = static_cast<uint32_t>(seed >> 32);
+  a.offset = offset;
+  a.inv_tau = 1.0f / temperature;
   return chain_draft_launch(a, reinterpret_cast<cudaStream_t>(stream));
 }
 

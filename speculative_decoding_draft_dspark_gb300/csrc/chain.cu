@@ -25,6 +25,12 @@
 // 32 rows and gathers their U rows.  The TMA producers do not depend on the winners and
 // keep streaming V and logits across position boundaries.
 //
+// Probabilistic drafting ("Adaptive Verification in vLLM", section "Appendix:
+// reproducing", draft_sample_method "probabilistic") is the same kernel with
+// SAMPLE set: the epilogue adds Gumbel noise from Philox4x32-10 to adj / tau
+// before the maximum (the Gumbel-max rule), so each token is a draw from the
+// softmax of the adjusted logits.
+//
 // Warp roles (256 threads, one CTA per SM, all 512 TMEM columns):
 //   warp 0      TMA producer of V tiles (4 K-blocks of 64 per tile)
 //   warp 1      TMEM allocation; one thread issues tcgen05.mma
@@ -83,7 +89,44 @@ struct ChainParams {
   int32_t n_mtiles, n_vgroups, n_quanta;
   int32_t l_k_is_dim1;  // logits map: dim1 = K, dim2 = N (else swapped)
   int32_t v_keep_tenths;
+  uint32_t seed_lo, seed_hi, offset;  // sampling: Philox key, counter word 3
+  float inv_tau;                       // sampling: 1 / temperature
 };
+
+// Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC 2011): 10 rounds of two 32 x 32 -> 64-bit products of
+// counter words 0 and 2 with the round multipliers, the high halves mixed
+// into the other words with the key, the key bumped by the Weyl constants.
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u;
+constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;
+constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
+
+__device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t k0,
+                                              uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t p0 = static_cast<uint64_t>(kPhiloxM0) * c[0];
+    const uint64_t p1 = static_cast<uint64_t>(kPhiloxM1) * c[2];
+    const uint32_t n0 = static_cast<uint32_t>(p1 >> 32) ^ c[1] ^ k0;
+    const uint32_t n2 = static_cast<uint32_t>(p0 >> 32) ^ c[3] ^ k1;
+    c[0] = n0;
+    c[1] = static_cast<uint32_t>(p1);
+    c[2] = n2;
+    c[3] = static_cast<uint32_t>(p0);
+    k0 += kPhiloxW0;
+    k1 += kPhiloxW1;
+  }
+}
+
+// Gumbel noise from one 32-bit word: u = (2 (x >> 9) + 1) 2^-24 (exact: the
+// mantissa trick gives 1 + (x >> 9) 2^-23, and subtracting 1 - 2^-24 is exact
+// by Sterbenz's lemma), g = -ln(-ln u).  ln is the accurate logf, which keeps
+// its relative accuracy for u next to 1.
+__device__ __forceinline__ float gumbel_from_word(uint32_t x) {
+  const float u = __uint_as_float(0x3F800000u | (x >> 9)) - 0x1.fffffep-1f;
+  return -logf(-logf(u));
+}
 
 // Tile i of position k over the quanta [qb, qe) a CTA owns: even positions
 // sweep upwards from qb, odd ones downwards from qe (the V tiles read last
@@ -159,7 +202,7 @@ __device__ __forceinline__ int decode_index(unsigned long long key, int vocab) {
   return idx;
 }
 
-template <int LDT>
+template <int LDT, bool SAMPLE>
 __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     chain_kernel(const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmL,
@@ -453,6 +496,20 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
               for (int e = 0; e < 32; ++e)
                 if (vbase + e >= p.vocab) v[e] = -INFINITY;
             }
+            if constexpr (SAMPLE) {
+              // Gumbel-max: key = adj / tau + g(n, k, v); word v % 4 of the
+              // Philox block with counter (v / 4, n, k, offset)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                uint32_t x[4] = {static_cast<uint32_t>(vbase >> 2) + i,
+                                 static_cast<uint32_t>(m), static_cast<uint32_t>(k),
+                                 p.offset};
+                philox4x32_10(x, p.seed_lo, p.seed_hi);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  v[4 * i + j] = fmaf(v[4 * i + j], p.inv_tau, gumbel_from_word(x[j]));
+              }
+            }
             float mx = v[0];
 #pragma unroll
             for (int e = 1; e < 32; ++e) mx = fmax_nan(mx, v[e]);
@@ -543,20 +600,31 @@ static EncodeTiledFn encode_tiled_fn() {
 }
 
 static std::mutex g_attr_mu;
-static bool g_attr_done[2][128];
+static bool g_attr_done[4][128];
 
 static cudaError_t ensure_kernel_attrs(int dev) {
   std::lock_guard<std::mutex> lk(g_attr_mu);
   if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  if (!g_attr_done[2][dev]) {
+    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DSPARK_BF16, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         CHAIN_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(chain_kernel<DSPARK_F32, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             CHAIN_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    g_attr_done[2][dev] = true;
+  }
   if (!g_attr_done[0][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DSPARK_BF16>,
+    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DSPARK_BF16, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          CHAIN_SMEM_BYTES);
     if (e != cudaSuccess) return e;
     g_attr_done[0][dev] = true;
   }
   if (!g_attr_done[1][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DSPARK_F32>,
+    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DSPARK_F32, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          CHAIN_SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -665,6 +733,10 @@ dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream) {
   p.n_vgroups = n_vgroups;
   p.n_quanta = n_quanta;
   p.l_k_is_dim1 = l_k_is_dim1;
+  p.seed_lo = a.seed_lo;
+  p.seed_hi = a.seed_hi;
+  p.offset = a.offset;
+  p.inv_tau = a.inv_tau;
   {
     const double v_bytes = static_cast<double>(a.vocab) * a.rank * 2;
     const int tenths = static_cast<int>(10.0 * kL2KeepBytes / v_bytes);
@@ -682,10 +754,17 @@ dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
-  if (a.logits_dtype == DSPARK_BF16)
-    e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_BF16>, tmV, tmL, p);
-  else
-    e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_F32>, tmV, tmL, p);
+  if (a.sample) {
+    if (a.logits_dtype == DSPARK_BF16)
+      e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_BF16, true>, tmV, tmL, p);
+    else
+      e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_F32, true>, tmV, tmL, p);
+  } else {
+    if (a.logits_dtype == DSPARK_BF16)
+      e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_BF16, false>, tmV, tmL, p);
+    else
+      e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_F32, false>, tmV, tmL, p);
+  }
   if (e == cudaErrorCooperativeLaunchTooLarge) return DSPARK_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return DSPARK_ERR_CUDA;
   return DSPARK_OK;

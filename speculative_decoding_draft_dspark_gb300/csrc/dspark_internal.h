@@ -32,6 +32,10 @@ struct ChainArgs {
   int32_t *draft;
   float *score;
   void *workspace;
+  // probabilistic drafting (Gumbel-max with Philox4x32-10 noise)
+  int32_t sample = 0;
+  uint32_t seed_lo = 0, seed_hi = 0, offset = 0;
+  float inv_tau = 1.0f;
 };
 size_t chain_workspace_bytes(int32_t N, int32_t K);
 dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream);

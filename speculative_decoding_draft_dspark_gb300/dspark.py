@@ -48,6 +48,9 @@ _SIGS = {
     "dspark_chain_workspace_size": (_SZ, [_I32, _I32]),
     "dspark_chain_draft": (_I32, [_P, _I32, _I64, _I64, _P, _P, _P, _I32, _I32,
                                   _I32, _I32, _P, _P, _P, _SZ, _P]),
+    "dspark_chain_sample": (_I32, [_P, _I32, _I64, _I64, _P, _P, _P, _I32, _I32,
+                                   _I32, _I32, ctypes.c_uint64, _U32, _F, _P,
+                                   _P, _P, _SZ, _P]),
     "dspark_chain_draft_noalloc": (_I32, [_P, _I32, _I64, _I64, _P, _P, _P,
                                           _I32, _I32, _I32, _I32, _P, _P, _P,
                                           _P]),
@@ -159,6 +162,30 @@ def dspark_chain_draft(logits, U, V, last_token, draft_tokens, draft_score,
         _ptr(draft_score), _ptr(workspace), _nbytes(workspace),
         _stream(stream))
     return _check("dspark_chain_draft", code, raise_on_error)
+
+
+def dspark_chain_sample(logits, U, V, last_token, draft_tokens, draft_score,
+                        workspace, *, seed, offset, temperature=1.0, N=None,
+                        K=None, vocab=None, rank=None, stride_n=None,
+                        stride_k=None, logits_dtype=None, stream=None,
+                        raise_on_error=True) -> int:
+    """dspark_chain_draft with Gumbel-max sampling (probabilistic drafting);
+    seed (uint64), offset (uint32) and temperature as in include/dspark.h."""
+    import torch
+    if logits_dtype is None:
+        logits_dtype = BF16 if logits.dtype == torch.bfloat16 else F32
+    N = logits.shape[0] if N is None else N
+    K = logits.shape[1] if K is None else K
+    vocab = logits.shape[2] if vocab is None else vocab
+    rank = U.shape[1] if rank is None else rank
+    stride_n = logits.stride(0) if stride_n is None else stride_n
+    stride_k = logits.stride(1) if stride_k is None else stride_k
+    code = load().dspark_chain_sample(
+        _ptr(logits), logits_dtype, stride_n, stride_k, _ptr(U), _ptr(V),
+        _ptr(last_token), N, K, vocab, rank, int(seed), int(offset),
+        float(temperature), _ptr(draft_tokens), _ptr(draft_score),
+        _ptr(workspace), _nbytes(workspace), _stream(stream))
+    return _check("dspark_chain_sample", code, raise_on_error)
 
 
 def dspark_chain_draft_noalloc(logits, U, V, last_token, draft_tokens,

@@ -37,8 +37,9 @@ def i32(n) -> torch.Tensor:
 # --------------------------------------------------------------- chain
 def run_chain(logits: np.ndarray, dtype: str, U: np.ndarray, V: np.ndarray,
               last: np.ndarray, layout: str = "nkv", pad: int = 0,
-              with_score: bool = True):
-    """Runs dspark_chain_draft; logits [N, K, vocab] stored in `layout`
+              with_score: bool = True, sample: dict | None = None):
+    """Runs dspark_chain_draft (or dspark_chain_sample with ``sample`` =
+    dict(seed, offset, tau)); logits [N, K, vocab] stored in `layout`
     ("nkv" row-major, "knv" position-major) with `pad` extra elements per
     innermost row.  Returns (draft, score, status)."""
     N, K, vocab = logits.shape
@@ -64,22 +65,43 @@ def run_chain(logits: np.ndarray, dtype: str, U: np.ndarray, V: np.ndarray,
     draft = torch.full((N, K), -1, dtype=torch.int32, device=DEV)
     score = torch.zeros(N, K, dtype=torch.float32, device=DEV) if with_score else None
     ws = D.new_workspace(D.dspark_chain_workspace_size(N, K), DEV)
-    D.dspark_chain_draft(t, up_bf16(U), up_bf16(V), up(last.astype(np.int32)),
-                         draft, score, ws, N=N, K=K, vocab=vocab,
-                         rank=U.shape[1], stride_n=stride_n, stride_k=stride_k,
-                         logits_dtype=D.BF16 if dtype == "bf16" else D.F32)
+    kw = dict(N=N, K=K, vocab=vocab, rank=U.shape[1], stride_n=stride_n,
+              stride_k=stride_k, logits_dtype=D.BF16 if dtype == "bf16" else D.F32)
+    if sample is None:
+        D.dspark_chain_draft(t, up_bf16(U), up_bf16(V), up(last.astype(np.int32)),
+                             draft, score, ws, **kw)
+    else:
+        D.dspark_chain_sample(t, up_bf16(U), up_bf16(V), up(last.astype(np.int32)),
+                              draft, score, ws, seed=sample["seed"],
+                              offset=sample["offset"], temperature=sample["tau"],
+                              **kw)
     torch.cuda.synchronize()
     st = D.dspark_read_status(ws)
     return (draft.cpu().numpy().astype(np.int64),
             None if score is None else score.cpu().numpy(), st)
 
 
-def check_chain(got, got_score, logits, dtype, U, V, last, rows=None):
+def check_chain(got, got_score, logits, dtype, U, V, last, rows=None,
+                sample=None):
     """Compares device tokens of `rows` (indices into logits' first axis)
-    with the oracle; returns the number of accepted near-tie divergences."""
+    with the oracle; returns the number of accepted near-tie divergences.
+    With ``sample`` the compared values are the Gumbel-perturbed ones
+    (adj / tau + noise of the row's own request index)."""
     rows = np.arange(logits.shape[0]) if rows is None else np.asarray(rows)
     sub = logits[rows]
-    ref = oracle.chain(sub, dtype, U, V, np.asarray(last)[rows])
+    ref = oracle.chain(sub, dtype, U, V, np.asarray(last)[rows], sample=sample,
+                       rows=rows)
+    vocab = logits.shape[2]
+
+    def position(i, k, prev):
+        noise, tau = None, 1.0
+        if sample is not None:
+            noise = oracle.gumbel_noise(int(sample["seed"]), int(sample["offset"]),
+                                        int(rows[i]), k, vocab)[None, :]
+            tau = float(sample["tau"])
+        return oracle.chain_position(oracle.to_f64(sub[i:i + 1, k, :], dtype),
+                                     U64, V64, np.array([prev]), noise, tau)
+
     g = got[rows]
     near = 0
     U64, V64 = oracle.bf16_to_f64(U), oracle.bf16_to_f64(V)
@@ -90,14 +112,13 @@ def check_chain(got, got_score, logits, dtype, U, V, last, rows=None):
             if not diverged:
                 if g[i, k] == ref["draft"][i, k]:
                     if got_score is not None:
-                        _score_ok(got_score[rows[i], k], ref["score"][i, k])
+                        _score_ok(got_score[rows[i], k], ref["score"][i, k],
+                                  floor=1e-3 if sample is None else 1.0)
                     continue
                 # tolerated only at a near-tie of the oracle's own values
                 mx, mg = ref["score"][i, k], ref["margin"][i, k]
                 tol = NEAR_TIE * abs(mx)
-                r = oracle.chain_position(
-                    oracle.to_f64(sub[i:i + 1, k, :], dtype), U64, V64,
-                    np.array([_prev(ref["draft"], last, rows, i, k)]))
+                r = position(i, k, _prev(ref["draft"], last, rows, i, k))
                 assert mg < tol and r["adj"][0, g[i, k]] >= mx - tol, \
                     (rows[i], k, g[i, k], ref["draft"][i, k], mx, mg)
                 near += 1
@@ -106,8 +127,7 @@ def check_chain(got, got_score, logits, dtype, U, V, last, rows=None):
                 continue
             # validity of the rest of a diverged row, given the device's
             # own previous token
-            r = oracle.chain_position(oracle.to_f64(sub[i:i + 1, k, :], dtype),
-                                      U64, V64, np.array([prev_tok]))
+            r = position(i, k, prev_tok)
             mx = r["score"][0]
             tol = NEAR_TIE * abs(mx)
             assert r["adj"][0, g[i, k]] >= mx - tol, (rows[i], k)
@@ -124,11 +144,11 @@ def _prev(draft, last, rows, i, k):
     return int(draft[i, k - 1])
 
 
-def _score_ok(got, want):
+def _score_ok(got, want, floor=1e-3):
     if np.isnan(want):
         assert np.isnan(got)
         return
-    assert abs(float(got) - want) <= SCORE_RTOL * max(abs(want), 1e-3), (got, want)
+    assert abs(float(got) - want) <= SCORE_RTOL * max(abs(want), floor), (got, want)
 
 
 # ----------------------------------------------------------- scheduler

@@ -17,7 +17,7 @@ def lib():
 
 def test_exports_every_header_function(lib):
     names = D.header_functions()
-    assert len(names) == 17
+    assert len(names) == 18
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(D._SIGS)
@@ -64,6 +64,26 @@ def _chain(lib, **kw):
 ])
 def test_chain_validation(lib, kw, code):
     assert _chain(lib, **kw) == code
+
+
+def test_chain_sample_validation(lib):
+    f = lib.dspark_chain_sample
+    ok = dict(logits=FAKE, dt=D.BF16, sn=1024 * 7, sk=1024, U=FAKE, V=FAKE,
+              last=FAKE, N=4, K=7, vocab=1024, rank=16, seed=1, offset=0,
+              tau=1.0, draft=FAKE, score=None, ws=FAKE * 2, wsb=1 << 16,
+              stream=None)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(*a.values())
+
+    for tau in (0.0, -1.0, float("nan"), float("inf"), 1e-45):
+        assert call(tau=tau) == D.ERR_INVALID_ARG, tau
+    assert call(logits=None) == D.ERR_INVALID_ARG
+    assert call(K=40) == D.ERR_UNSUPPORTED
+    assert call(rank=24) == D.ERR_UNSUPPORTED
+    assert call(wsb=16) == D.ERR_WORKSPACE
 
 
 def test_select_validation(lib):
