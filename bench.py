@@ -547,6 +547,17 @@ def run_sample_chain(st, cfg, stream, iters=50):
     elems = cfg.N * cfg.K * cfg.vocab
     out["elements"] = elems
     out["gelem_per_s"] = round(elems / (out["sample_us"] * 1e-6) / 1e9, 2)
+    # ALU roofline: per element, a quarter of a Philox4x32-10 block (10 rounds
+    # of 2 wide multiplies and 2 three-input XORs = 40 ops per 4 elements),
+    # the adjusted-logit add and the comparison: 12 integer / fp32 ops; peak
+    # = 128 such ops per SM per clock at the 2070 MHz maximum SM clock
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    peak_tops = sms * 128 * 2.070e9 / 1e12
+    achieved = elems * 12 / (out["sample_us"] * 1e-6) / 1e12
+    out["roofline"] = {"bound": "alu", "ops_per_element": 12,
+                       "achieved": round(achieved, 2), "peak": round(peak_tops, 2),
+                       "unit": "Tops/s", "frac": round(achieved / peak_tops, 4),
+                       "peak_source": "derived: SMs x 128 lanes x 2070 MHz"}
     out["note"] = ("dspark_chain_sample vs dspark_chain_draft, back-to-back "
                    "launches; not part of the step metric")
     return out

@@ -31,13 +31,16 @@
 // before the maximum (the Gumbel-max rule), so each token is a draw from the
 // softmax of the adjusted logits.
 //
-// Warp roles (256 threads, one CTA per SM, all 512 TMEM columns):
+// Warp roles (one CTA per SM, all 512 TMEM columns):
 //   warp 0      TMA producer of V tiles (4 K-blocks of 64 per tile)
 //   warp 1      TMEM allocation; one thread issues tcgen05.mma
 //   warp 2      TMA producer of logits boxes
 //   warp 3      idle
 //   warps 4-7   grid barrier, winner decode and U gather, then the epilogue
 //               (TMEM lane quarter w % 4)
+//   warps 8-19  sampling only: more epilogue warps on the same lane quarters
+//               (warp w takes lane quarter w % 4), the four warps of a
+//               quarter splitting each tile's 32-column chunks
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
@@ -67,7 +70,12 @@ constexpr int SMEM_BAR_OFF = SMEM_L_OFF + NUM_L_STAGES * L_STAGE_BYTES;
 constexpr int NUM_BARS = 20;
 constexpr int SMEM_USED = SMEM_BAR_OFF + NUM_BARS * 8 + 16;
 constexpr int CHAIN_SMEM_BYTES = SMEM_USED + 1024;  // 1 KB alignment slack
-constexpr int CHAIN_THREADS = 256;
+// warps 0-3 have fixed roles; EPI epilogue warps follow (4 for the argmax
+// chain, 16 for sampling, whose epilogue does far more arithmetic per element:
+// measured at the headline size, 8 / 12 / 16 warps take 1543 / 1441 / 1325 us)
+constexpr int chain_threads(int epi) { return (4 + epi) * 32; }
+constexpr int EPI_ARGMAX = 4;
+constexpr int EPI_SAMPLE = 16;
 constexpr uint32_t TMEM_COLS = 512;  // two 256-column fp32 accumulators
 // bytes of V worth protecting in L2 across positions (measured on GB300:
 // protecting more than this lets the logits stream evict it anyway)
@@ -102,20 +110,32 @@ constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
 constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;
 constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
 
-__device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t k0,
-                                              uint32_t k1) {
+// The round keys depend only on the seed: a thread computes them once.
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+
+__device__ __forceinline__ PhiloxKeys philox_keys(uint32_t k0, uint32_t k1) {
+  PhiloxKeys r;
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    r.k0[i] = k0 + static_cast<uint32_t>(i) * kPhiloxW0;
+    r.k1[i] = k1 + static_cast<uint32_t>(i) * kPhiloxW1;
+  }
+  return r;
+}
+
+__device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], const PhiloxKeys &key) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
     const uint64_t p0 = static_cast<uint64_t>(kPhiloxM0) * c[0];
     const uint64_t p1 = static_cast<uint64_t>(kPhiloxM1) * c[2];
-    const uint32_t n0 = static_cast<uint32_t>(p1 >> 32) ^ c[1] ^ k0;
-    const uint32_t n2 = static_cast<uint32_t>(p0 >> 32) ^ c[3] ^ k1;
+    const uint32_t n0 = static_cast<uint32_t>(p1 >> 32) ^ c[1] ^ key.k0[r];
+    const uint32_t n2 = static_cast<uint32_t>(p0 >> 32) ^ c[3] ^ key.k1[r];
     c[0] = n0;
     c[1] = static_cast<uint32_t>(p1);
     c[2] = n2;
     c[3] = static_cast<uint32_t>(p0);
-    k0 += kPhiloxW0;
-    k1 += kPhiloxW1;
   }
 }
 
@@ -123,6 +143,12 @@ __device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t k0,
 // mantissa trick gives 1 + (x >> 9) 2^-23, and subtracting 1 - 2^-24 is exact
 // by Sterbenz's lemma), g = -ln(-ln u).  ln is the accurate logf, which keeps
 // its relative accuracy for u next to 1.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float gumbel_from_word(uint32_t x) {
   const float u = __uint_as_float(0x3F800000u | (x >> 9)) - 0x1.fffffep-1f;
   return -logf(-logf(u));
@@ -164,16 +190,17 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity,
 }
 
 // An epilogue warp waits until every epilogue warp of the CTAs sharing its
-// 128-request tile has published position k (4 arrivals per CTA; the tiles
-// are independent chains).  Lane 0 polls with a time limit; the warp leaves
+// 128-request tile has published position k (one arrival per epilogue warp
+// and CTA; the tiles are independent chains).  Lane 0 polls with a time limit; the warp leaves
 // together.  No barrier spans warps, so a warp that gives up can never leave
 // another one blocked.
 __device__ __forceinline__ bool grid_wait(const ChainParams &p, int k,
                                           int m_tile,
-                                          volatile uint32_t *cta_abort) {
+                                          volatile uint32_t *cta_abort,
+                                          uint32_t arrivals_per_cta) {
   uint32_t r = 1;
   if ((threadIdx.x & 31) == 0) {
-    const uint32_t target = 4u * static_cast<uint32_t>(p.n_vgroups) +
+    const uint32_t target = arrivals_per_cta * static_cast<uint32_t>(p.n_vgroups) +
                             (*p.hang_test != 0u ? 1u : 0u);
     const uint32_t *cnt = &p.counters[k * p.n_mtiles + m_tile];
     if (ld_acquire_gpu(cnt) < target) {
@@ -202,8 +229,8 @@ __device__ __forceinline__ int decode_index(unsigned long long key, int vocab) {
   return idx;
 }
 
-template <int LDT, bool SAMPLE>
-__global__ void __launch_bounds__(CHAIN_THREADS, 1)
+template <int LDT, bool SAMPLE, int EPI>
+__global__ void __launch_bounds__(chain_threads(EPI), 1)
     chain_kernel(const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmL,
                  const ChainParams p) {
@@ -246,13 +273,13 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
     }
     for (int i = 0; i < NUM_L_STAGES; ++i) {
       mbar_init(&l_full[i], 1);
-      mbar_init(&l_empty[i], 4);
+      mbar_init(&l_empty[i], EPI);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
+      mbar_init(&acc_empty[i], EPI);
     }
-    mbar_init(a_full, 4);
+    mbar_init(a_full, 4);  // the first four epilogue warps gather A
     mbar_init(mma_done, 1);
     *abort_flag = 0u;
     fence_mbarrier_init();
@@ -382,10 +409,16 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
   } else if (warp >= 4) {
     // ----------------------------- grid barrier, gather, epilogue per k
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // sub-group: with more than four epilogue warps, warps sharing a lane
+    // quarter split each tile's 32-column chunks; sub-group 0 alone waits at
+    // the grid barrier, decodes the winners and gathers U
+    const int sg = (warp - 4) >> 2;
+    constexpr int NSG = EPI / 4;
     const int row = q * 32 + lane;
     const int m = m0 + row;
     const bool row_ok = m < p.N;
-    const bool writer = (grp == 0) && row_ok;  // one CTA per tile writes draft
+    const bool writer = (grp == 0) && row_ok && sg == 0;  // one CTA per tile writes draft
+    [[maybe_unused]] const PhiloxKeys pkeys = philox_keys(p.seed_lo, p.seed_hi);
     const uint32_t a_base = smem_u32(smem + SMEM_A_OFF);
     int ig = 0, lit = 0;
     bool ok = true;
@@ -399,8 +432,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             raise_status(p.status, DSPARK_DEV_TOKEN_OOR);
           }
         }
-      } else {
-        if (!(ok = grid_wait(p, k - 1, m_tile, abort_flag))) break;
+      } else if (sg == 0) {
+        if (!(ok = grid_wait(p, k - 1, m_tile, abort_flag, EPI))) break;
         if (row_ok) {
           const unsigned long long key = *reinterpret_cast<volatile unsigned long long *>(
               &p.slots[static_cast<size_t>(k - 1) * p.N + m]);
@@ -417,8 +450,8 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
       // gather this position's U rows into A, one 512-byte row per warp
       // instruction (lane j copies 16-byte chunk j of the row); the MMAs of
       // position k-1 have all retired, their last accumulator was consumed
-      const int nchunk = KB * 8;
-      for (int r = 0; r < 32; ++r) {
+      const int nchunk = sg == 0 ? KB * 8 : 0;
+      for (int r = 0; r < 32 && sg == 0; ++r) {
         const int rp = __shfl_sync(0xFFFFFFFFu, prev, r);
         const int rrow = q * 32 + r;
         const bool rok = (m0 + rrow) < p.N;
@@ -432,14 +465,17 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
             st_shared_zero16(dst);
         }
       }
-      cp_async_commit();
-      cp_async_wait_all();
-      fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
-      __syncwarp();
-      if (lane == 0) mbar_arrive(a_full);
+      if (sg == 0) {
+        cp_async_commit();
+        cp_async_wait_all();
+        fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(a_full);
+      }
 
       uint32_t best_key = 0u;  // below every real key
       int best_idx = 0x7FFFFFFF;
+      float best_val = -INFINITY;  // the value behind best_key (sampling)
       for (int i = 0; i < nt && ok; ++i, ++ig) {
         const TileGeom g = tile_geom(k, i, qb, qe);
         const int buf = ig & 1;
@@ -459,73 +495,139 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
               smem_u32(smem + SMEM_L_OFF + s * L_STAGE_BYTES) + row * 128;
 #pragma unroll
           for (int c = 0; c < CHUNKS_PER_BOX; ++c) {
+            if (NSG > 1 && (j * CHUNKS_PER_BOX + c) % NSG != sg) continue;
             const int col0 = j * LBOX_COLS + c * 32;
-            uint32_t acc[32];
-            tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(buf * BN + col0),
-                               acc);
-            tmem_ld_wait(acc);
-            float v[32];
-            if constexpr (LDT == DSPARK_BF16) {
+            if constexpr (SAMPLE) {
+              // Gumbel-max: key = adj / tau + g(n, k, v), g from word v % 4
+              // of the Philox block with counter (v / 4, n, k, offset).  An
+              // element can beat the running best only if g > best - adj/tau
+              // - margin, i.e. 1 - u < 1 - exp(-A) <= A with
+              // A = exp(adj/tau - best + margin).  1 - u is exact from the
+              // inverted word, so the test costs one ex2 and no logarithm;
+              // the (1 + 2^-10) factor and the margin cover every rounding
+              // and approximation error, so a skipped element could never
+              // have won.  Survivors get the exact key.  The chunk is taken
+              // 8 columns at a time in a rolled loop: the fully unrolled form
+              // does not fit the instruction cache.
+              const float s1 = p.inv_tau * 1.4426950408889634f;
+#pragma unroll 1
+              for (int h = 0; h < 4; ++h) {
+                const int cb = col0 + h * 8;
+                uint32_t acc[8];
+                tmem_ld_32x32b_x8(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                      static_cast<uint32_t>(buf * BN + cb),
+                                  acc);
+                tmem_ld_wait(acc);
+                float v[8];
+                if constexpr (LDT == DSPARK_BF16) {
+                  const int chunk = c * 4 + h;
+                  const uint4 w = ld_shared_v4(box + ((chunk ^ (row & 7)) << 4));
+                  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int chunk = c * 4 + u;
-                const uint4 w = ld_shared_v4(box + ((chunk ^ (row & 7)) << 4));
-                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                  for (int t = 0; t < 4; ++t) {
+                    v[2 * t] = __uint_as_float(acc[2 * t]) + __uint_as_float(ww[t] << 16);
+                    v[2 * t + 1] = __uint_as_float(acc[2 * t + 1]) +
+                                   __uint_as_float(ww[t] & 0xFFFF0000u);
+                  }
+                } else {
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                  v[u * 8 + 2 * h] = __uint_as_float(acc[u * 8 + 2 * h]) +
-                                     __uint_as_float(ww[h] << 16);
-                  v[u * 8 + 2 * h + 1] = __uint_as_float(acc[u * 8 + 2 * h + 1]) +
-                                         __uint_as_float(ww[h] & 0xFFFF0000u);
+                  for (int t = 0; t < 2; ++t) {
+                    const int chunk = 2 * h + t;
+                    const uint4 w = ld_shared_v4(box + ((chunk ^ (row & 7)) << 4));
+                    v[4 * t + 0] = __uint_as_float(acc[4 * t + 0]) + __uint_as_float(w.x);
+                    v[4 * t + 1] = __uint_as_float(acc[4 * t + 1]) + __uint_as_float(w.y);
+                    v[4 * t + 2] = __uint_as_float(acc[4 * t + 2]) + __uint_as_float(w.z);
+                    v[4 * t + 3] = __uint_as_float(acc[4 * t + 3]) + __uint_as_float(w.w);
+                  }
+                }
+                const int vb = v_tile0 + cb;
+                if (vb + 8 > p.vocab) {
+#pragma unroll
+                  for (int e = 0; e < 8; ++e)
+                    if (vb + e >= p.vocab) v[e] = -INFINITY;
+                }
+                const bool none = best_key == 0u || best_val != best_val;
+                const float margin = 1e-4f * (1.0f + fabsf(best_val));
+                const float s0 = none ? INFINITY
+                                      : (margin - best_val) * 1.4426950408889634f + 0x1p-10f;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                  uint32_t x[4] = {static_cast<uint32_t>(vb >> 2) + i,
+                                   static_cast<uint32_t>(m), static_cast<uint32_t>(k),
+                                   p.offset};
+                  philox4x32_10(x, pkeys);
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    const float A = ex2_approx(fmaf(v[4 * i + j], s1, s0));
+                    const float w = __uint_as_float(0x3F800000u | (~x[j] >> 9)) - 0x1.fffffep-1f;
+                    const bool cand = !(w >= A);  // NaN adj or best: always
+                    if (__any_sync(0xFFFFFFFFu, cand) && cand) {
+                      const float key = fmaf(v[4 * i + j], p.inv_tau, gumbel_from_word(x[j]));
+                      const uint32_t kk = f32_key(key);
+                      const int idx = vb + 4 * i + j;
+                      if (kk > best_key || (kk == best_key && idx < best_idx)) {
+                        best_key = kk;
+                        best_idx = idx;
+                        best_val = key;
+                      }
+                    }
+                  }
                 }
               }
             } else {
+              uint32_t acc[32];
+              tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                     static_cast<uint32_t>(buf * BN + col0),
+                                 acc);
+              tmem_ld_wait(acc);
+              float v[32];
+              if constexpr (LDT == DSPARK_BF16) {
 #pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const uint4 w = ld_shared_v4(box + ((u ^ (row & 7)) << 4));
-                v[u * 4 + 0] = __uint_as_float(acc[u * 4 + 0]) + __uint_as_float(w.x);
-                v[u * 4 + 1] = __uint_as_float(acc[u * 4 + 1]) + __uint_as_float(w.y);
-                v[u * 4 + 2] = __uint_as_float(acc[u * 4 + 2]) + __uint_as_float(w.z);
-                v[u * 4 + 3] = __uint_as_float(acc[u * 4 + 3]) + __uint_as_float(w.w);
+                for (int u = 0; u < 4; ++u) {
+                  const int chunk = c * 4 + u;
+                  const uint4 w = ld_shared_v4(box + ((chunk ^ (row & 7)) << 4));
+                  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                  for (int h = 0; h < 4; ++h) {
+                    v[u * 8 + 2 * h] = __uint_as_float(acc[u * 8 + 2 * h]) +
+                                       __uint_as_float(ww[h] << 16);
+                    v[u * 8 + 2 * h + 1] = __uint_as_float(acc[u * 8 + 2 * h + 1]) +
+                                           __uint_as_float(ww[h] & 0xFFFF0000u);
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                  const uint4 w = ld_shared_v4(box + ((u ^ (row & 7)) << 4));
+                  v[u * 4 + 0] = __uint_as_float(acc[u * 4 + 0]) + __uint_as_float(w.x);
+                  v[u * 4 + 1] = __uint_as_float(acc[u * 4 + 1]) + __uint_as_float(w.y);
+                  v[u * 4 + 2] = __uint_as_float(acc[u * 4 + 2]) + __uint_as_float(w.z);
+                  v[u * 4 + 3] = __uint_as_float(acc[u * 4 + 3]) + __uint_as_float(w.w);
+                }
               }
-            }
-            const int vbase = v_tile0 + col0;
-            if (vbase + 32 > p.vocab) {
+              const int vbase = v_tile0 + col0;
+              if (vbase + 32 > p.vocab) {
 #pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (vbase + e >= p.vocab) v[e] = -INFINITY;
-            }
-            if constexpr (SAMPLE) {
-              // Gumbel-max: key = adj / tau + g(n, k, v); word v % 4 of the
-              // Philox block with counter (v / 4, n, k, offset)
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                uint32_t x[4] = {static_cast<uint32_t>(vbase >> 2) + i,
-                                 static_cast<uint32_t>(m), static_cast<uint32_t>(k),
-                                 p.offset};
-                philox4x32_10(x, p.seed_lo, p.seed_hi);
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  v[4 * i + j] = fmaf(v[4 * i + j], p.inv_tau, gumbel_from_word(x[j]));
+                for (int e = 0; e < 32; ++e)
+                  if (vbase + e >= p.vocab) v[e] = -INFINITY;
               }
-            }
-            float mx = v[0];
+              float mx = v[0];
 #pragma unroll
-            for (int e = 1; e < 32; ++e) mx = fmax_nan(mx, v[e]);
-            int ie = 0;
-            if (mx != mx) {
+              for (int e = 1; e < 32; ++e) mx = fmax_nan(mx, v[e]);
+              int ie = 0;
+              if (mx != mx) {
 #pragma unroll
-              for (int e = 31; e >= 0; --e) ie = (v[e] != v[e]) ? e : ie;
-            } else {
+                for (int e = 31; e >= 0; --e) ie = (v[e] != v[e]) ? e : ie;
+              } else {
 #pragma unroll
-              for (int e = 31; e >= 0; --e) ie = (v[e] == mx) ? e : ie;
-            }
-            const uint32_t key = f32_key(mx);
-            const int idx = vbase + ie;
-            if (key > best_key || (key == best_key && idx < best_idx)) {
-              best_key = key;
-              best_idx = idx;
+                for (int e = 31; e >= 0; --e) ie = (v[e] == mx) ? e : ie;
+              }
+              const uint32_t key = f32_key(mx);
+              const int idx = vbase + ie;
+              if (key > best_key || (key == best_key && idx < best_idx)) {
+                best_key = key;
+                best_idx = idx;
+              }
             }
           }
           __syncwarp();
@@ -549,9 +651,9 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
       __syncwarp();
       if (lane == 0) atomicAdd(&p.counters[k * p.n_mtiles + m_tile], 1u);
     }
-    if (ok) {
+    if (ok && sg == 0) {
       // winners of the last position
-      ok = grid_wait(p, p.K - 1, m_tile, abort_flag);
+      ok = grid_wait(p, p.K - 1, m_tile, abort_flag, EPI);
       if (ok && writer) {
         const unsigned long long key = *reinterpret_cast<volatile unsigned long long *>(
             &p.slots[static_cast<size_t>(p.K - 1) * p.N + m]);
@@ -606,25 +708,25 @@ static cudaError_t ensure_kernel_attrs(int dev) {
   std::lock_guard<std::mutex> lk(g_attr_mu);
   if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
   if (!g_attr_done[2][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DSPARK_BF16, true>,
+    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DSPARK_BF16, true, EPI_SAMPLE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          CHAIN_SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(chain_kernel<DSPARK_F32, true>,
+    e = cudaFuncSetAttribute(chain_kernel<DSPARK_F32, true, EPI_SAMPLE>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              CHAIN_SMEM_BYTES);
     if (e != cudaSuccess) return e;
     g_attr_done[2][dev] = true;
   }
   if (!g_attr_done[0][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DSPARK_BF16, false>,
+    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DSPARK_BF16, false, EPI_ARGMAX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          CHAIN_SMEM_BYTES);
     if (e != cudaSuccess) return e;
     g_attr_done[0][dev] = true;
   }
   if (!g_attr_done[1][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DSPARK_F32, false>,
+    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DSPARK_F32, false, EPI_ARGMAX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          CHAIN_SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -745,7 +847,7 @@ dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream) {
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(CHAIN_THREADS);
+  cfg.blockDim = dim3(chain_threads(a.sample ? EPI_SAMPLE : EPI_ARGMAX));
   cfg.dynamicSmemBytes = CHAIN_SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -756,14 +858,14 @@ dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream) {
   cudaError_t e;
   if (a.sample) {
     if (a.logits_dtype == DSPARK_BF16)
-      e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_BF16, true>, tmV, tmL, p);
+      e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_BF16, true, EPI_SAMPLE>, tmV, tmL, p);
     else
-      e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_F32, true>, tmV, tmL, p);
+      e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_F32, true, EPI_SAMPLE>, tmV, tmL, p);
   } else {
     if (a.logits_dtype == DSPARK_BF16)
-      e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_BF16, false>, tmV, tmL, p);
+      e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_BF16, false, EPI_ARGMAX>, tmV, tmL, p);
     else
-      e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_F32, false>, tmV, tmL, p);
+      e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_F32, false, EPI_ARGMAX>, tmV, tmL, p);
   }
   if (e == cudaErrorCooperativeLaunchTooLarge) return DSPARK_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return DSPARK_ERR_CUDA;
