@@ -424,6 +424,7 @@ def run_gpu(args):
             result["next_greedy_verify"] = run_greedy_verify(st, cfg, stream)
             result["next_stale_select"] = run_stale_select(st, cfg, stream)
             result["next_sample_chain"] = run_sample_chain(st, cfg, stream)
+            result["next_lmhead_chain"] = run_lmhead_chain(st, cfg, stream)
         if world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(cfg)
         print(json.dumps(result), flush=True)
@@ -561,6 +562,54 @@ def run_sample_chain(st, cfg, stream, iters=50):
     out["note"] = ("dspark_chain_sample vs dspark_chain_draft, back-to-back "
                    "launches; not part of the step metric")
     return out
+
+
+def run_lmhead_chain(st, cfg, stream, iters=20):
+    """Fused output projection (not part of the metric): dspark_chain_lmhead
+    on hidden states h [N, K, d] and a projection W [vocab, d] (d = 2048)
+    instead of stored logits; CUDA events over back-to-back launches."""
+    import numpy as np
+    import torch
+    import workloads
+    D = st.D
+    x = workloads.make_lmhead_inputs(cfg)
+    dev = st.logits.device
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)  # noqa: E731
+    h, W = bf(x["h"]), bf(x["W"])
+    del x
+
+    def one():
+        D.dspark_chain_lmhead(h, W, st.U, st.V, st.last, st.draft, st.score, st.cws)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one()
+    stream.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        s.record(stream)
+        for _ in range(iters):
+            one()
+        e.record(stream)
+    stream.synchronize()
+    us = s.elapsed_time(e) * 1e3 / iters
+    d = W.shape[1]
+    flops = 2.0 * cfg.N * cfg.K * cfg.vocab * (d + cfg.rank)
+    # W and V streamed once per position (neither fits in L2), h once
+    hbm = cfg.K * cfg.vocab * (d + cfg.rank) * 2 + cfg.N * cfg.K * d * 2
+    hbm_peak, tf_peak, _, src = measured_peaks()
+    tf = flops / (us * 1e-6) / 1e12
+    gbs = hbm / (us * 1e-6) / 1e9
+    return {"us": round(us, 2), "d": d, "flops_per_launch": flops,
+            "hbm_bytes_per_launch": hbm,
+            "roofline_tensor": {"achieved": round(tf, 1), "peak": tf_peak,
+                                "unit": "TFLOP/s", "frac": round(tf / tf_peak, 4)},
+            "roofline_hbm": {"achieved": round(gbs, 1), "peak": hbm_peak,
+                             "unit": "GB/s", "frac": round(gbs / hbm_peak, 4)},
+            "peak_source": src,
+            "note": "dspark_chain_lmhead (h . W^T + U[prev] . V^T, logits never "
+                    "stored), not part of the step metric"}
 
 
 def run_e2e(st, cfg, stream, steps):

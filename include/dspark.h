@@ -152,6 +152,31 @@ DSPARK_API dspark_status dspark_chain_sample(
     void *workspace, size_t workspace_bytes, dspark_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Fused output projection.  "DSpark on MAX", "What DSpark is", items 2-3:
+ * the block drafter scores all K positions in one pass and the chain adds
+ * the low-rank bias before the argmax.  This call takes the drafter's hidden
+ * states and output projection instead of its logits and computes
+ *     adj[n,k,v] = h[n,k,:] . W[v,:] + U[prev] . V[v,:]
+ * as one product with inner dimension d + rank (bf16 operands, fp32
+ * accumulation), so the backbone logits are never written to memory.  The
+ * chain, argmax rule, status bits, workspace and limits are those of
+ * dspark_chain_draft.
+ * h           bf16 [N, K, d]; element (n, k, j) at n*h_stride_n +
+ *             k*h_stride_k + j (elements); strides multiples of 8, base
+ *             16-byte aligned.
+ * W           bf16 [vocab, d] row-major, 16-byte aligned.
+ * d           a multiple of 64 in [64, 65536]; vocab a multiple of 8.
+ * draft_score optional out [N, K]: adj at draft[n,k].
+ * ------------------------------------------------------------------------ */
+DSPARK_API dspark_status dspark_chain_lmhead(
+    const void *h, int64_t h_stride_n, int64_t h_stride_k,
+    const void *W, const void *U, const void *V,
+    const int32_t *last_token,
+    int32_t N, int32_t K, int32_t vocab, int32_t d, int32_t rank,
+    int32_t *draft_tokens, float *draft_score,
+    void *workspace, size_t workspace_bytes, dspark_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * dspark_chain_draft for callers that cannot allocate device memory.  The
  * pages have no counterpart: this is an interface convenience, not part of
  * the method.  Code running inside a CUDA graph capture, serving engines

@@ -32,6 +32,11 @@ What it computes, step by step, with the passage each step follows:
   allocation uses current confidences; "How DSpark Speeds Up LLM Inference",
   appendix Part B: capacity from confidences two steps earlier): the budget
   steps run on the older buffer, the order and allocation on the current one.
+* Fused LM head ("DSpark on MAX", *What DSpark is*, items 2-3: the block
+  drafter emits scores for all K positions in one pass, then the chain adds
+  the low-rank bias): the backbone logits are h[n, k] . W^T for hidden
+  states h and the drafter's output projection W, computed here in fp64 and
+  fed to the same chain.
 * Greedy verification ("DSpark on MAX", *The kernel pass*, item 2): a draft
   token is accepted iff it equals the target's best token; the longest
   accepted run is kept and the target's next token is added.
@@ -430,3 +435,20 @@ def select_step_stale(conf_size, conf, mask, cost, T, draft_cost=0.0, flags=0,
                 f=sized["f"], draft_len=ln, cu_len=cp["cu_len"],
                 verify_idx=cp["verify_idx"], verify_tok=cp["verify_tok"],
                 cost_used=sized["cost_used"], status=st | sized["status"])
+
+
+def lmhead_logits(h: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """Backbone logits [n, K, vocab] (fp64) from bf16 hidden states h
+    [n, K, d] and the bf16 output projection W [vocab, d]."""
+    h64 = bf16_to_f64(h)
+    W64 = bf16_to_f64(W)
+    return h64 @ W64.T
+
+
+def chain_lmhead(h: np.ndarray, W: np.ndarray, U: np.ndarray, V: np.ndarray,
+                 last_token: np.ndarray, rows: np.ndarray | None = None) -> dict:
+    """The chain over adj = h . W^T + U[prev] . V^T ("DSpark on MAX", *What
+    DSpark is*, items 2-3): the drafter's output projection and the Markov
+    bias as one score, the backbone logits never stored on the device.  All
+    of h, W, U, V are bf16 bit patterns; ``rows`` as for chain()."""
+    return chain(lmhead_logits(h, W), "f64", U, V, last_token, rows=rows)

@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdspark.so")
-SOURCES = ["chain.cu", "select.cu", "verify.cu", "api.cu", "chain_noalloc.cu"]
+SOURCES = ["chain.cu", "lmhead.cu", "select.cu", "verify.cu", "api.cu", "chain_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr"]

@@ -209,6 +209,52 @@ dspark_status dspark_chain_sample(const void *logits, int32_t logits_dtype,
   return chain_draft_launch(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+dspark_status dspark_chain_lmhead(const void *h, int64_t h_stride_n,
+                                  int64_t h_stride_k, const void *W,
+                                  const void *U, const void *V,
+                                  const int32_t *last_token, int32_t N,
+                                  int32_t K, int32_t vocab, int32_t d,
+                                  int32_t rank, int32_t *draft_tokens,
+                                  float *draft_score, void *workspace,
+                                  size_t workspace_bytes,
+                                  dspark_stream_t stream) {
+  if (!h || !W || !U || !V || !last_token || !draft_tokens)
+    return DSPARK_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0 || vocab <= 0 || d <= 0 || rank <= 0)
+    return DSPARK_ERR_INVALID_ARG;
+  if (K > kMaxK) return DSPARK_ERR_UNSUPPORTED;
+  if (rank % 16 != 0 || rank > 256) return DSPARK_ERR_UNSUPPORTED;
+  if (d % 64 != 0 || d > 65536) return DSPARK_ERR_UNSUPPORTED;
+  if (vocab < 8 || vocab % 8 != 0) return DSPARK_ERR_UNSUPPORTED;
+  if (h_stride_n < d || h_stride_n % 8 != 0) return DSPARK_ERR_INVALID_ARG;
+  if (K > 1 && (h_stride_k < d || h_stride_k % 8 != 0)) return DSPARK_ERR_INVALID_ARG;
+  if (!aligned(h, 16) || !aligned(W, 16) || !aligned(U, 16) || !aligned(V, 16))
+    return DSPARK_ERR_INVALID_ARG;
+  if (!aligned(last_token, 4) || !aligned(draft_tokens, 4) ||
+      (draft_score && !aligned(draft_score, 4)))
+    return DSPARK_ERR_INVALID_ARG;
+  const dspark_status s =
+      check_ws(workspace, workspace_bytes, chain_workspace_bytes(N, K));
+  if (s != DSPARK_OK) return s;
+  LmheadArgs a;
+  a.h = h;
+  a.stride_n = h_stride_n;
+  a.stride_k = h_stride_k;
+  a.W = W;
+  a.U = U;
+  a.V = V;
+  a.last_token = last_token;
+  a.N = N;
+  a.K = K;
+  a.vocab = vocab;
+  a.d = d;
+  a.rank = rank;
+  a.draft = draft_tokens;
+  a.score = draft_score;
+  a.workspace = workspace;
+  return lmhead_chain_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t dspark_select_workspace_size(int32_t N, int32_t K, int32_t cost_len) {
   if (N <= 0 || K <= 0 || cost_len <= 0) return 0;
   return kSelectWorkspaceBytes;

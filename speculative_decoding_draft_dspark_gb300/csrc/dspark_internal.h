@@ -17,6 +17,10 @@ constexpr size_t kChainSlotsOffset = 256;   // uint64 [K][N] per-row winners,
                                             // then uint32 [K][N/128] counters
 constexpr size_t kSelectWorkspaceBytes = 256;
 
+inline size_t chain_counters_offset(int32_t N, int32_t K) {
+  return kChainSlotsOffset + static_cast<size_t>(N) * K * 8;
+}
+
 constexpr int kMaxK = 32;
 constexpr int kMaxSlots = 16384;  // N*K limit of the scheduler kernels
 
@@ -38,6 +42,18 @@ struct ChainArgs {
   float inv_tau = 1.0f;
 };
 size_t chain_workspace_bytes(int32_t N, int32_t K);
+
+struct LmheadArgs {
+  const void *h;  // bf16 [N, K, d] (strides in elements)
+  int64_t stride_n, stride_k;
+  const void *W, *U, *V;  // bf16 [vocab, d], [vocab, rank], [vocab, rank]
+  const int32_t *last_token;
+  int32_t N, K, vocab, d, rank;
+  int32_t *draft;
+  float *score;
+  void *workspace;
+};
+dspark_status lmhead_chain_launch(const LmheadArgs &a, cudaStream_t stream);
 dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream);
 
 struct SelectArgs {

@@ -51,6 +51,8 @@ _SIGS = {
     "dspark_chain_sample": (_I32, [_P, _I32, _I64, _I64, _P, _P, _P, _I32, _I32,
                                    _I32, _I32, ctypes.c_uint64, _U32, _F, _P,
                                    _P, _P, _SZ, _P]),
+    "dspark_chain_lmhead": (_I32, [_P, _I64, _I64, _P, _P, _P, _P, _I32, _I32,
+                                   _I32, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "dspark_chain_draft_noalloc": (_I32, [_P, _I32, _I64, _I64, _P, _P, _P,
                                           _I32, _I32, _I32, _I32, _P, _P, _P,
                                           _P]),
@@ -186,6 +188,25 @@ def dspark_chain_sample(logits, U, V, last_token, draft_tokens, draft_score,
         float(temperature), _ptr(draft_tokens), _ptr(draft_score),
         _ptr(workspace), _nbytes(workspace), _stream(stream))
     return _check("dspark_chain_sample", code, raise_on_error)
+
+
+def dspark_chain_lmhead(h, W, U, V, last_token, draft_tokens, draft_score,
+                        workspace, *, N=None, K=None, d=None, stride_n=None,
+                        stride_k=None, stream=None, raise_on_error=True) -> int:
+    """Chain over h . W^T + U[prev] . V^T: h [N, K, d] bf16 hidden states
+    (or any layout given by N, K, d and the element strides), W [vocab, d]
+    bf16 output projection, U/V [vocab, rank] bf16."""
+    N = h.shape[0] if N is None else N
+    K = h.shape[1] if K is None else K
+    d = W.shape[1] if d is None else d
+    vocab, rank = W.shape[0], U.shape[1]
+    stride_n = h.stride(0) if stride_n is None else stride_n
+    stride_k = h.stride(1) if stride_k is None else stride_k
+    code = load().dspark_chain_lmhead(
+        _ptr(h), stride_n, stride_k, _ptr(W), _ptr(U), _ptr(V),
+        _ptr(last_token), N, K, vocab, d, rank, _ptr(draft_tokens),
+        _ptr(draft_score), _ptr(workspace), _nbytes(workspace), _stream(stream))
+    return _check("dspark_chain_lmhead", code, raise_on_error)
 
 
 def dspark_chain_draft_noalloc(logits, U, V, last_token, draft_tokens,

@@ -17,7 +17,7 @@ def lib():
 
 def test_exports_every_header_function(lib):
     names = D.header_functions()
-    assert len(names) == 18
+    assert len(names) == 19
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(D._SIGS)
@@ -83,6 +83,29 @@ def test_chain_sample_validation(lib):
     assert call(logits=None) == D.ERR_INVALID_ARG
     assert call(K=40) == D.ERR_UNSUPPORTED
     assert call(rank=24) == D.ERR_UNSUPPORTED
+    assert call(wsb=16) == D.ERR_WORKSPACE
+
+
+def test_chain_lmhead_validation(lib):
+    f = lib.dspark_chain_lmhead
+    ok = dict(h=FAKE, sn=7 * 2048, sk=2048, W=FAKE, U=FAKE, V=FAKE, last=FAKE,
+              N=4, K=7, vocab=1024, d=2048, rank=16, draft=FAKE, score=None,
+              ws=FAKE * 2, wsb=1 << 16, stream=None)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(*a.values())
+
+    assert call(h=None) == D.ERR_INVALID_ARG
+    assert call(W=None) == D.ERR_INVALID_ARG
+    assert call(d=100) == D.ERR_UNSUPPORTED           # not a multiple of 64
+    assert call(d=0) == D.ERR_INVALID_ARG
+    assert call(rank=300) == D.ERR_UNSUPPORTED
+    assert call(vocab=1020) == D.ERR_UNSUPPORTED
+    assert call(sn=2047) == D.ERR_INVALID_ARG
+    assert call(sk=2044) == D.ERR_INVALID_ARG
+    assert call(h=FAKE + 8) == D.ERR_INVALID_ARG       # misaligned
     assert call(wsb=16) == D.ERR_WORKSPACE
 
 

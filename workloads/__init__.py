@@ -283,6 +283,21 @@ def make_chain_factors(cfg: Config) -> dict:
     return dict(U=U, V=V, tie_pairs=pairs)
 
 
+# width of the drafter's output projection for the fused LM-head workloads
+# (a drafter of about a billion parameters; the pages give no width)
+LMHEAD_D = 2048
+
+
+def make_lmhead_inputs(cfg: Config, d: int = LMHEAD_D) -> dict:
+    """Hidden states h [N, K, d] ~ N(0, 1) and output projection W [vocab, d]
+    ~ N(0, logit_sd / sqrt(d)), both bf16 bits, so that h . W^T has the
+    workload's logit spread; drawn from a seed sequence of their own."""
+    kids = np.random.SeedSequence([cfg.seed, 0x4C4D]).spawn(2)
+    h = _normal_bf16_blocked(kids[0], cfg.N * cfg.K, d, 1.0).reshape(cfg.N, cfg.K, d)
+    W = _normal_bf16_blocked(kids[1], cfg.vocab, d, cfg.logit_sd / np.sqrt(d))
+    return dict(h=h, W=W, d=d)
+
+
 def make_last_token(cfg: Config) -> np.ndarray:
     rng = np.random.default_rng(_streams(cfg.seed)[_S_LAST])
     return rng.integers(0, cfg.vocab, size=cfg.N, dtype=np.int64).astype(np.int32)
