@@ -50,8 +50,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-graph", action="store_true",
                     help="launch eagerly instead of replaying CUDA graphs")
-    ap.add_argument("--no-verify", action="store_true",
-                    help="skip the extra greedy-verification measurement")
+    ap.add_argument("--no-extras", "--no-verify", dest="no_extras", action="store_true",
+                    help="skip the measurements of the NEXT rows (greedy verify, stale sizing, sampling, fused output projection)")
     ap.add_argument("--serial", action="store_true",
                     help="run the scheduler after the chain on one stream "
                          "instead of alongside it")
@@ -420,7 +420,7 @@ def run_gpu(args):
     }
     if rank == 0:
         result["e2e"] = run_e2e(st, cfg, stream, args.e2e_steps)
-        if not args.no_verify:
+        if not args.no_extras:
             result["next_greedy_verify"] = run_greedy_verify(st, cfg, stream)
             result["next_stale_select"] = run_stale_select(st, cfg, stream)
             result["next_sample_chain"] = run_sample_chain(st, cfg, stream)
