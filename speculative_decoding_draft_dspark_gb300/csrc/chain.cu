@@ -38,9 +38,9 @@
 //   warp 3      idle
 //   warps 4-7   grid barrier, winner decode and U gather, then the epilogue
 //               (TMEM lane quarter w % 4)
-//   warps 8-19  sampling only: more epilogue warps on the same lane quarters
-//               (warp w takes lane quarter w % 4), the four warps of a
-//               quarter splitting each tile's 32-column chunks
+//   warps 8-11  more epilogue warps on the same lane quarters (warp w takes
+//               quarter w % 4; the warps of a quarter split each tile's
+//               32-column chunks); sampling runs warps 8-19
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
@@ -66,11 +66,12 @@ constexpr int SMEM_BAR_OFF = SMEM_L_OFF + NUM_L_STAGES * L_STAGE_BYTES;
 constexpr int NUM_BARS = 20;
 constexpr int SMEM_USED = SMEM_BAR_OFF + NUM_BARS * 8 + 16;
 constexpr int CHAIN_SMEM_BYTES = SMEM_USED + 1024;  // 1 KB alignment slack
-// warps 0-3 have fixed roles; EPI epilogue warps follow (4 for the argmax
-// chain, 16 for sampling, whose epilogue does far more arithmetic per element:
-// measured at the headline size, 8 / 12 / 16 warps take 1543 / 1441 / 1325 us)
+// warps 0-3 have fixed roles; EPI epilogue warps follow: 8 for the argmax
+// chain (4 / 8 / 12 measured at the headline: chain 311 / 295 / 301 us;
+// Stress 2410 / 2176 / 2157 us), 16 for sampling, whose epilogue does far
+// more arithmetic per element (8 / 12 / 16: 1543 / 1441 / 1325 us)
 constexpr int chain_threads(int epi) { return (4 + epi) * 32; }
-constexpr int EPI_ARGMAX = 4;
+constexpr int EPI_ARGMAX = 8;
 constexpr int EPI_SAMPLE = 16;
 constexpr uint32_t TMEM_COLS = 512;  // two 256-column fp32 accumulators
 // bytes of V worth protecting in L2 across positions (measured on GB300:
