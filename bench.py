@@ -615,48 +615,86 @@ def run_lmhead_chain(st, cfg, stream, iters=20):
 def run_e2e(st, cfg, stream, steps):
     """The same step through the public API with host buffers: per step the
     inputs are copied from pinned host memory and the scheduler's results
-    are read back, all inside the timed region."""
+    are read back, all inside the timed region.  Two device buffer sets let
+    the copy engine fill step i+1's inputs while the GPU computes step i
+    (host-to-device on one copy stream, device-to-host on another)."""
     import numpy as np
     import torch
+    D = st.D
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
     h_logits = pin(st.logits_np.view(np.int16) if cfg.logits_dtype == "bf16" else st.logits_np)
     h_conf, h_mask = pin(st.sel["conf"]), pin(st.sel["mask"])
     h_last = pin(st.last_np)
     h_T = torch.tensor([st.sel["T"]], dtype=torch.int32).pin_memory()
-    outs = [st.B, st.ln, st.cu, st.vi, st.vt, st.draft]
-    h_outs = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
-    d_logits_raw = st.logits.view(torch.int16) if cfg.logits_dtype == "bf16" else st.logits
-    h2d = sum(t.numel() * t.element_size() for t in (h_logits, h_conf, h_mask, h_last, h_T))
-    d2h = sum(t.numel() * t.element_size() for t in h_outs)
+    h_in = (h_logits, h_conf, h_mask, h_last, h_T)
 
-    def one():
-        d_logits_raw.copy_(h_logits, non_blocking=True)
-        st.conf.copy_(h_conf, non_blocking=True)
-        st.mask.copy_(h_mask, non_blocking=True)
-        st.last.copy_(h_last, non_blocking=True)
-        st.T.copy_(h_T, non_blocking=True)
-        st.chain()
-        st.select()
-        for d, h in zip(outs, h_outs):
-            h.copy_(d, non_blocking=True)
+    base = dict(logits=st.logits, conf=st.conf, mask=st.mask, last=st.last,
+                T=st.T, draft=st.draft, score=st.score, surv=st.surv, srt=st.srt,
+                pre=st.pre, ne=st.ne, ns=st.ns, B=st.B, obj=st.obj, ln=st.ln,
+                cu=st.cu, vi=st.vi, vt=st.vt)
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            one()
-    stream.synchronize()
+    def buffers(first):
+        d = dict(base) if first else {k: torch.empty_like(v) for k, v in base.items()}
+        d["in"] = (d["logits"].view(torch.int16) if cfg.logits_dtype == "bf16"
+                   else d["logits"], d["conf"], d["mask"], d["last"], d["T"])
+        d["outs"] = [d["B"], d["ln"], d["cu"], d["vi"], d["vt"], d["draft"]]
+        d["h_outs"] = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in d["outs"]]
+        return d
+
+    sets = [buffers(True), buffers(False)]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in sets[0]["h_outs"])
+    cs, ds = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("h2d", "comp", "d2h")}
+    started = [False, False]
+
+    def one(i):
+        j = i % 2
+        b = sets[j]
+        if started[j]:
+            cs.wait_event(ev["comp"][j])   # step i-2 has finished reading set j
+        with torch.cuda.stream(cs):
+            for d_t, h_t in zip(b["in"], h_in):
+                d_t.copy_(h_t, non_blocking=True)
+            ev["h2d"][j].record(cs)
+        stream.wait_event(ev["h2d"][j])
+        if started[j]:
+            stream.wait_event(ev["d2h"][j])  # step i-2's results are read back
+        with torch.cuda.stream(stream):
+            D.dspark_chain_draft(b["logits"], st.U, st.V, b["last"], b["draft"],
+                                 b["score"], st.cws)
+            D.dspark_select_step(b["conf"], b["mask"], st.cost, b["T"], 0.0,
+                                 st.flags, b["draft"], b["surv"], b["srt"], b["pre"],
+                                 b["ne"], b["ns"], b["B"], b["obj"], b["ln"],
+                                 b["cu"], b["vi"], b["vt"], st.sws)
+            ev["comp"][j].record(stream)
+        ds.wait_event(ev["comp"][j])
+        with torch.cuda.stream(ds):
+            for d_t, h_t in zip(b["outs"], b["h_outs"]):
+                h_t.copy_(d_t, non_blocking=True)
+            ev["d2h"][j].record(ds)
+        started[j] = True
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        s.record(stream)
-        for _ in range(steps):
-            one()
-        e.record(stream)
-    stream.synchronize()
+    s.record(stream)
+    cs.wait_event(s)  # the first copy starts after the start stamp
+    for i in range(steps):
+        one(i)
+    for j in range(2):
+        stream.wait_event(ev["d2h"][j])
+    e.record(stream)
+    torch.cuda.synchronize()
     us = s.elapsed_time(e) * 1e3 / steps
     return {"value": round(us, 2), "unit": "us/step", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps,
-            "path": "pinned host -> device copies, dspark_chain_draft, "
-                    "dspark_select_step, device -> pinned host copies"}
+            "path": "pinned host -> device copies (copy stream), dspark_chain_draft, "
+                    "dspark_select_step, device -> pinned host copies (second copy "
+                    "stream); two device buffer sets so step i+1's copy overlaps "
+                    "step i's compute"}
 
 
 # ------------------------------------------------------- CPU oracle leg
