@@ -69,7 +69,7 @@ constexpr int CHAIN_SMEM_BYTES = SMEM_USED + 1024;  // 1 KB alignment slack
 // warps 0-3 have fixed roles; EPI epilogue warps follow: 8 for the argmax
 // chain (4 / 8 / 12 measured at the headline: chain 311 / 295 / 301 us;
 // Stress 2410 / 2176 / 2157 us), 16 for sampling, whose epilogue does far
-// more arithmetic per element (8 / 12 / 16: 1543 / 1441 / 1325 us)
+// more arithmetic per element (8 / 12 / 16 / 20: 870 / 822 / 807 / 869 us)
 constexpr int chain_threads(int epi) { return (4 + epi) * 32; }
 constexpr int EPI_ARGMAX = 8;
 constexpr int EPI_SAMPLE = 16;
@@ -472,26 +472,43 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                 const float margin = 1e-4f * (1.0f + fabsf(best_val));
                 const float s0 = none ? INFINITY
                                       : (margin - best_val) * 1.4426950408889634f + 0x1p-10f;
+                uint32_t x[8];
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
-                  uint32_t x[4] = {static_cast<uint32_t>(vb >> 2) + i,
-                                   static_cast<uint32_t>(m), static_cast<uint32_t>(k),
-                                   p.offset};
-                  philox4x32_10(x, pkeys);
+                  uint32_t w4[4] = {static_cast<uint32_t>(vb >> 2) + i,
+                                    static_cast<uint32_t>(m), static_cast<uint32_t>(k),
+                                    p.offset};
+                  philox4x32_10(w4, pkeys);
 #pragma unroll
-                  for (int j = 0; j < 4; ++j) {
-                    const float A = ex2_approx(fmaf(v[4 * i + j], s1, s0));
-                    const float w = __uint_as_float(0x3F800000u | (~x[j] >> 9)) - 0x1.fffffep-1f;
-                    const bool cand = !(w >= A);  // NaN adj or best: always
-                    if (__any_sync(0xFFFFFFFFu, cand) && cand) {
-                      const float key = fmaf(v[4 * i + j], p.inv_tau, gumbel_from_word(x[j]));
-                      const uint32_t kk = f32_key(key);
-                      const int idx = vb + 4 * i + j;
-                      if (kk > best_key || (kk == best_key && idx < best_idx)) {
-                        best_key = kk;
-                        best_idx = idx;
-                        best_val = key;
-                      }
+                  for (int j = 0; j < 4; ++j) x[4 * i + j] = w4[j];
+                }
+                uint32_t cand = 0u;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const float A = ex2_approx(fmaf(v[e], s1, s0));
+                  const float w = __uint_as_float(0x3F800000u | (~x[e] >> 9)) - 0x1.fffffep-1f;
+                  cand |= (!(w >= A) ? 1u : 0u) << e;  // NaN adj or best: always
+                }
+                // survivors, lowest column first, through one copy of the
+                // exact key (a few per thousand elements)
+                if (__any_sync(0xFFFFFFFFu, cand != 0u)) {
+                  while (cand != 0u) {
+                    const int e = __ffs(cand) - 1;
+                    cand &= cand - 1u;
+                    float ve = v[0];
+                    uint32_t xe = x[0];
+#pragma unroll
+                    for (int t = 1; t < 8; ++t) {
+                      ve = e == t ? v[t] : ve;
+                      xe = e == t ? x[t] : xe;
+                    }
+                    const float key = fmaf(ve, p.inv_tau, gumbel_from_word(xe));
+                    const uint32_t kk = f32_key(key);
+                    const int idx = vb + e;
+                    if (kk > best_key || (kk == best_key && idx < best_idx)) {
+                      best_key = kk;
+                      best_idx = idx;
+                      best_val = key;
                     }
                   }
                 }
