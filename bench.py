@@ -360,7 +360,7 @@ def run_gpu(args):
     step_us = [ev[i][0].elapsed_time(ev[i][3]) * 1e3 for i in range(K_steps)]
     total_ms = max_over_ranks(total_ms, dev)
 
-    # outputs of the timed steps are still the oracle's (cheap integrity check)
+    # the timed steps raised no device status bit (cheap integrity check)
     assert D.dspark_read_status(st.cws) == 0 and D.dspark_read_status(st.sws) == 0
 
     ms_per_iter = total_ms / K_steps
@@ -373,6 +373,8 @@ def run_gpu(args):
     traffic = recorded_traffic()
     q = lambda xs, p: float(np.percentile(np.array(xs), p))  # noqa: E731
 
+    v_streamed_bytes = (algorithmic_bytes_per_launch(cfg)
+                        + (cfg.K - 1) * cfg.vocab * cfg.rank * 2)
     result = {
         "metric": METRIC, "value": round(value_us, 3), "unit": "us/step",
         "n_gpus": world, "steps": K_steps, "warmup": W,
@@ -406,6 +408,10 @@ def run_gpu(args):
             "frac": round(achieved_gbs / hbm, 4), "traffic": traffic,
             "algorithmic_bytes_per_launch": algorithmic_bytes_per_launch(cfg),
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+            # V re-read at every position (the bound when no V line survives
+            # in L2 between positions): context for frac, not the roofline
+            "v_streamed_bytes_per_launch": v_streamed_bytes,
+            "frac_v_streamed": round(v_streamed_bytes / (chain_med * 1e-6) / 1e9 / hbm, 4),
         },
         "roofline_tensor": {
             "bound": "tensor", "achieved": round(achieved_tf, 2),
