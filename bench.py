@@ -258,7 +258,13 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
-    __graft_entry__.build()
+    # one process compiles the in-tree library; the others wait and load it
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+        if rank != 0:
+            __graft_entry__.build()  # up to date by now: only loads
     cfg = workloads.get_config(args.workload)
     st = Step(cfg, dev)
     D = st.D
