@@ -127,3 +127,32 @@ def test_verify_k32_smallest_vocabulary():
     np.testing.assert_array_equal(acc.cpu().numpy(), ref["accepted"])
     np.testing.assert_array_equal(bon.cpu().numpy(), ref["bonus"])
     assert D.dspark_read_status(ws) == 0
+
+
+def test_special_values_and_odd_position_ties():
+    """Ties at odd positions (the vocabulary is swept downwards there, so the
+    lower index is met last), +inf pairs, NaN beating +inf, and NaN reaching
+    a column through the bias (a NaN in a V row)."""
+    from gpu_harness import run_chain
+    from speculative_decoding_draft_dspark_gb300 import dspark as D
+    N, K, vocab, rank = 5, 4, 40960, 32     # many tiles per CTA at every position
+    logits, U, V, last = _chain_inputs(N, K, vocab, rank, "f32", seed=21)
+    V[33000] = V[1000]                      # identical bias for columns 1000 / 33000
+    for k in (1, 3):                        # odd positions: downward sweep
+        logits[0, k, 1000] = logits[0, k, 33000] = 60.0
+    logits[1, 1, 5000] = logits[1, 1, 39000] = np.inf
+    logits[2, 3, 7000] = np.inf
+    logits[2, 3, 20000] = np.nan            # NaN outranks +inf
+    Vf = workloads.bf16_bits_to_f32(V).copy()
+    Vf[12345, 3] = np.nan                   # column 12345 is NaN for every row
+    Vn = workloads.f32_to_bf16_bits(Vf)
+    got, score, st = run_chain(logits, "f32", U, V, last)
+    ref = oracle.chain(logits, "f32", U, V, last)
+    np.testing.assert_array_equal(got, ref["draft"])
+    assert got[0, 1] == 1000 and got[0, 3] == 1000
+    assert got[1, 1] == 5000 and score[1, 1] == np.inf
+    assert got[2, 3] == 20000
+    got2, _, st2 = run_chain(logits, "f32", U, Vn, last)
+    ref2 = oracle.chain(logits, "f32", U, Vn, last)
+    np.testing.assert_array_equal(got2, ref2["draft"])
+    assert np.all(got2 == 12345) and st2 & D.DEV_NAN_LOGIT
