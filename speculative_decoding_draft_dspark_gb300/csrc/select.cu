@@ -366,109 +366,95 @@ __device__ __forceinline__ double f64_from_key(unsigned long long k) {
 }
 
 // ------------------------------------------------------------------------
-// bitonic sort of P2 (key, slot) pairs in shared memory into priority order
-// (larger key first, then smaller slot).  Thread t holds elements
-// [t*E, t*E+E) in registers: strides below E are compare-exchanges inside a
-// thread, strides below 32*E exchange with a lane of the same warp, only
-// larger strides go through shared memory (one barrier each).
+// global priority order (larger key first, then smaller slot) of NK slots
+// whose keys come as sorted runs of K: the slots of one request, because a
+// survival never increases along a request (s[k+1] = s[k] * c with
+// 0 <= c <= 1, and rounding is monotone) and equal keys keep slot order.
+// Level l merges neighbouring runs of K * 2^l (merge path): every thread
+// writes ceil(NK / blockDim) consecutive outputs, finding how many of them
+// come from the left run by a binary search (the co-rank) and then merging
+// sequentially.  Only 16-bit slot ids move (between sidx and stmp); keys
+// stay indexed by slot.  n log2(n / K) steps in log2(NK / K) levels, against
+// n log2(n)^2 / 4 compare-exchanges in about log2(n)^2 / 2 stages for a
+// bitonic network.  On return sidx[0 .. NK) is the order and keys[0 .. NK)
+// the keys in that order.
 // ------------------------------------------------------------------------
 __device__ __forceinline__ bool prio_first(unsigned long long ka, uint32_t sa,
                                            unsigned long long kb, uint32_t sb) {
   return ka > kb || (ka == kb && sa < sb);
 }
 
-template <int E>
-__device__ void block_bitonic(unsigned long long *keys, uint16_t *sidx,
-                              const int P2) {
+constexpr int kMaxPerThread = (kMaxSlots + SEL_THREADS - 1) / SEL_THREADS;
+
+__device__ void block_merge_runs(unsigned long long *keys, uint16_t *sidx,
+                                 uint16_t *stmp, const int NK, const int K) {
   const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const bool active = tid < P2 / E;  // whole warps (P2 / E is a multiple of 32)
-  unsigned long long k[E];
-  uint32_t v[E];
-  if (active) {
-#pragma unroll
-    for (int j = 0; j < E; ++j) {
-      k[j] = keys[tid * E + j];
-      v[j] = sidx[tid * E + j];
+  const int NT = blockDim.x;
+  const int C = (NK + NT - 1) / NT;
+  const int p0 = min(NK, tid * C), p1 = min(NK, p0 + C);
+  uint16_t *src = sidx, *dst = stmp;
+  for (int i = tid; i < NK; i += NT) sidx[i] = static_cast<uint16_t>(i);
+  __syncthreads();
+  for (int L = K; L < NK; L <<= 1) {
+    int p = p0;
+    while (p < p1) {
+      // the pair of runs [base, base + L) and [base + L, base + 2L) holding p
+      const int base = p - p % (2 * L);
+      const int a_len = min(L, NK - base);
+      const int b0 = base + a_len;
+      const int b_len = min(L, NK - b0);
+      const uint16_t *A = src + base;
+      const uint16_t *B = src + b0;
+      const int q = p - base;
+      // co-rank: the number of A's elements among the pair's first q outputs
+      int lo = max(0, q - b_len), hi = min(q, a_len);
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        const uint32_t x = A[mid], y = B[q - mid - 1];
+        if (prio_first(keys[x], x, keys[y], y))
+          lo = mid + 1;
+        else
+          hi = mid;
+      }
+      int ia = lo, ib = q - lo;
+      // heads of both runs; an exhausted run's head is never taken (its
+      // index is clamped so the read stays inside the run)
+      uint32_t xa = A[min(ia, a_len - 1)];
+      uint32_t xb = b_len > 0 ? B[min(ib, b_len - 1)] : 0u;
+      unsigned long long ka = keys[xa], kb = keys[xb];
+      const int stop = min(p1, b0 + b_len);
+      for (; p < stop; ++p) {
+        const bool take_a = ia < a_len && (ib >= b_len || prio_first(ka, xa, kb, xb));
+        dst[p] = static_cast<uint16_t>(take_a ? xa : xb);
+        ia += take_a ? 1 : 0;
+        ib += take_a ? 0 : 1;
+        // refill the head that moved, without a branch
+        const uint16_t *next = take_a ? A + min(ia, a_len - 1) : B + min(ib, max(b_len - 1, 0));
+        const uint32_t x = *next;
+        const unsigned long long kx = keys[x];
+        xa = take_a ? x : xa;
+        ka = take_a ? kx : ka;
+        xb = take_a ? xb : x;
+        kb = take_a ? kb : kx;
+      }
     }
+    __syncthreads();
+    uint16_t *t = src;
+    src = dst;
+    dst = t;
   }
-  for (int s = 2; s <= P2; s <<= 1) {
-    int d = s >> 1;
-    if (d >= 32 * E) {  // shared-memory passes
-      if (active) {
+  // keys into sorted order: every thread reads its outputs' keys before any
+  // thread writes
+  unsigned long long kv[kMaxPerThread];
 #pragma unroll
-        for (int j = 0; j < E; ++j) {
-          keys[tid * E + j] = k[j];
-          sidx[tid * E + j] = static_cast<uint16_t>(v[j]);
-        }
-      }
-      __syncthreads();
-      for (; d >= 32 * E; d >>= 1) {
-        for (int i = tid; i < (P2 >> 1); i += blockDim.x) {
-          const int lo = ((i & ~(d - 1)) << 1) | (i & (d - 1));
-          const int hi = lo + d;
-          const unsigned long long ka = keys[lo], kb = keys[hi];
-          const uint16_t ia = sidx[lo], ib = sidx[hi];
-          const bool up = (lo & s) == 0;
-          if (up != prio_first(ka, ia, kb, ib)) {
-            keys[lo] = kb;
-            keys[hi] = ka;
-            sidx[lo] = ib;
-            sidx[hi] = ia;
-          }
-        }
-        __syncthreads();
-      }
-      if (active) {
+  for (int c = 0; c < kMaxPerThread; ++c)
+    if (p0 + c < p1) kv[c] = keys[src[p0 + c]];
+  __syncthreads();
 #pragma unroll
-        for (int j = 0; j < E; ++j) {
-          k[j] = keys[tid * E + j];
-          v[j] = sidx[tid * E + j];
-        }
-      }
-    }
-    if (active) {
-      for (; d >= E; d >>= 1) {  // partner in the same warp
-        const int m = d / E;
-        const bool lower = (lane & m) == 0;
-#pragma unroll
-        for (int j = 0; j < E; ++j) {
-          const int i = tid * E + j;
-          const unsigned long long pk = __shfl_xor_sync(0xFFFFFFFFu, k[j], m);
-          const uint32_t pv = __shfl_xor_sync(0xFFFFFFFFu, v[j], m);
-          const bool keep_first = lower == ((i & s) == 0);
-          if (keep_first != prio_first(k[j], v[j], pk, pv)) {
-            k[j] = pk;
-            v[j] = pv;
-          }
-        }
-      }
-#pragma unroll
-      for (int dd = E / 2; dd >= 1; dd >>= 1) {  // partner in this thread
-        if (dd > d) continue;
-#pragma unroll
-        for (int j = 0; j < E; ++j) {
-          if (j & dd) continue;
-          const int jj = j | dd;
-          const int i = tid * E + j;
-          const bool up = (i & s) == 0;
-          if (up != prio_first(k[j], v[j], k[jj], v[jj])) {
-            const unsigned long long tk = k[j];
-            const uint32_t tv = v[j];
-            k[j] = k[jj];
-            v[j] = v[jj];
-            k[jj] = tk;
-            v[jj] = tv;
-          }
-        }
-      }
-    }
-  }
-  if (active) {
-#pragma unroll
-    for (int j = 0; j < E; ++j) {
-      keys[tid * E + j] = k[j];
-      sidx[tid * E + j] = static_cast<uint16_t>(v[j]);
+  for (int c = 0; c < kMaxPerThread; ++c) {
+    if (p0 + c < p1) {
+      keys[p0 + c] = kv[c];
+      if (src != sidx) sidx[p0 + c] = src[p0 + c];
     }
   }
   __syncthreads();
@@ -480,13 +466,12 @@ __device__ void block_bitonic(unsigned long long *keys, uint16_t *sidx,
 constexpr int kMaxChunk = (kMaxSlots + 1 + SEL_THREADS - 1) / SEL_THREADS + 1;
 
 // Survival products of `conf` (fp64, left to right, clamped), sort keys
-// (bits(s) + 1, 0 for non-sampling requests) and the bitonic order.  With
+// (bits(s) + 1, 0 for non-sampling requests) and the merged order.  With
 // `outputs`, writes survival, sorted_slots, n_eligible and n_sampling.
-template <int E>
 __device__ void survival_order(const SelectArgs &a, const float *conf,
                                const bool outputs, unsigned long long *keys,
-                               uint16_t *sidx, const int P2, int *sh_int,
-                               int &n_s, uint32_t &st) {
+                               uint16_t *sidx, uint16_t *stmp, const int P2,
+                               int *sh_int, int &n_s, uint32_t &st) {
   const int tid = threadIdx.x;
   const int NT = blockDim.x;
   const int N = a.N, K = a.K, NK = N * K;
@@ -509,18 +494,13 @@ __device__ void survival_order(const SelectArgs &a, const float *conf,
       keys[n * K + k] =
           samp ? static_cast<unsigned long long>(__double_as_longlong(prod)) + 1ull
                : 0ull;
-      sidx[n * K + k] = static_cast<uint16_t>(n * K + k);
     }
   }
-  for (int i = NK + tid; i < P2; i += NT) {
-    keys[i] = 0ull;
-    sidx[i] = 0xFFFFu;
-  }
+  for (int i = NK + tid; i < P2; i += NT) keys[i] = 0ull;
   n_s = block_reduce(my_ns, OpAddInt(), 0, sh_int);
   const int S = n_s * K;
 
-  __syncthreads();
-  block_bitonic<E>(keys, sidx, P2);
+  block_merge_runs(keys, sidx, stmp, NK, K);
   if (outputs) {
     if (a.sorted_slots)
       for (int j = tid; j < S; j += NT) a.sorted_slots[j] = sidx[j];
@@ -531,12 +511,12 @@ __device__ void survival_order(const SelectArgs &a, const float *conf,
   }
 }
 
-template <int E>
 __global__ void __launch_bounds__(SEL_THREADS, 1)
     select_kernel(const SelectArgs a, const uint32_t stages, const int P2) {
   extern __shared__ __align__(16) uint8_t dsm[];
   unsigned long long *keys = reinterpret_cast<unsigned long long *>(dsm);  // [P2+1]
   uint16_t *sidx = reinterpret_cast<uint16_t *>(keys + P2 + 1);           // [P2]
+  uint16_t *stmp = sidx + P2;                                             // [P2]
   double *Pd = reinterpret_cast<double *>(keys);  // after the scan: P_{j+1}
   int *len_sm = reinterpret_cast<int *>(dsm);     // after the budget
 
@@ -560,8 +540,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   const bool stale = a.conf_size != nullptr && (stages & kStageSurvival) &&
                      (stages & kStageBudget) && (stages & kStageAllocate);
   if (stages & kStageSurvival) {
-    survival_order<E>(a, stale ? a.conf_size : a.conf, !stale, keys, sidx, P2,
-                      sh_int, n_s, st);
+    survival_order(a, stale ? a.conf_size : a.conf, !stale, keys, sidx, stmp, P2,
+                   sh_int, n_s, st);
     S = n_s * K;
 
     // exact prefix sums of the sorted survivals
@@ -729,7 +709,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     // them): order the current confidences for the allocation
     __syncthreads();
     int n_s2 = 0;
-    survival_order<E>(a, a.conf, true, keys, sidx, P2, sh_int, n_s2, st);
+    survival_order(a, a.conf, true, keys, sidx, stmp, P2, sh_int, n_s2, st);
     if (tid == 0) sh_B = min(sh_B, n_s2 * K);
     __syncthreads();
   }
@@ -833,19 +813,6 @@ static int next_pow2(int x) {
   return p;
 }
 
-template <int E>
-static cudaError_t set_select_attr() {
-  return cudaFuncSetAttribute(select_kernel<E>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              200 * 1024);
-}
-
-template <int E>
-static cudaError_t launch_select(const SelectArgs &a, uint32_t stages, int P2,
-                                 size_t dyn, cudaStream_t stream) {
-  select_kernel<E><<<1, SEL_THREADS, dyn, stream>>>(a, stages, P2);
-  return cudaGetLastError();
-}
 
 dspark_status select_launch(const SelectArgs &a, uint32_t stages,
                             cudaStream_t stream) {
@@ -855,11 +822,8 @@ dspark_status select_launch(const SelectArgs &a, uint32_t stages,
   {
     std::lock_guard<std::mutex> lk(g_sel_mu);
     if (!g_sel_attr[dev]) {
-      if (set_select_attr<1>() != cudaSuccess ||
-          set_select_attr<2>() != cudaSuccess ||
-          set_select_attr<4>() != cudaSuccess ||
-          set_select_attr<8>() != cudaSuccess ||
-          set_select_attr<16>() != cudaSuccess)
+      if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               200 * 1024) != cudaSuccess)
         return DSPARK_ERR_CUDA;
       g_sel_attr[dev] = true;
     }
@@ -869,24 +833,15 @@ dspark_status select_launch(const SelectArgs &a, uint32_t stages,
   size_t dyn = 0;
   if (stages & kStageSurvival) {
     P2 = next_pow2(NK < 64 ? 64 : NK);
-    dyn = static_cast<size_t>(P2 + 1) * 8 + static_cast<size_t>(P2) * 2;
+    dyn = static_cast<size_t>(P2 + 1) * 8 + static_cast<size_t>(P2) * 4;
   }
   if (stages & kStageAllocate) {
     const size_t need = static_cast<size_t>(a.N) * 4;
     if (need > dyn) dyn = need;
   }
   dyn = (dyn + 15) & ~static_cast<size_t>(15);
-  // elements per thread of the sort: P2 / 1024, at least 1
-  const int E = P2 > SEL_THREADS ? P2 / SEL_THREADS : 1;
-  cudaError_t e;
-  switch (E) {
-    case 1: e = launch_select<1>(a, stages, P2, dyn, stream); break;
-    case 2: e = launch_select<2>(a, stages, P2, dyn, stream); break;
-    case 4: e = launch_select<4>(a, stages, P2, dyn, stream); break;
-    case 8: e = launch_select<8>(a, stages, P2, dyn, stream); break;
-    case 16: e = launch_select<16>(a, stages, P2, dyn, stream); break;
-    default: return DSPARK_ERR_UNSUPPORTED;
-  }
+  select_kernel<<<1, SEL_THREADS, dyn, stream>>>(a, stages, P2);
+  const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
 
