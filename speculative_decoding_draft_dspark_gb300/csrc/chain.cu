@@ -40,7 +40,7 @@
 //               (TMEM lane quarter w % 4)
 //   warps 8-11  more epilogue warps on the same lane quarters (warp w takes
 //               quarter w % 4; the warps of a quarter split each tile's
-//               32-column chunks); sampling runs warps 8-19
+//               32-column chunks); sampling runs warps 8-15
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
@@ -72,7 +72,8 @@ constexpr int CHAIN_SMEM_BYTES = SMEM_USED + 1024;  // 1 KB alignment slack
 // more arithmetic per element (8 / 12 / 16 / 20: 870 / 822 / 807 / 869 us)
 constexpr int chain_threads(int epi) { return (4 + epi) * 32; }
 constexpr int EPI_ARGMAX = 8;
-constexpr int EPI_SAMPLE = 16;
+constexpr int EPI_SAMPLE = 12;
+constexpr int SAMPLE_PW = 16;  // columns per step of the sampling epilogue
 constexpr uint32_t TMEM_COLS = 512;  // two 256-column fp32 accumulators
 // bytes of V worth protecting in L2 across positions (measured on GB300:
 // protecting more than this lets the logits stream evict it anyway)
@@ -144,6 +145,20 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// hi32(a * b) + c in one instruction on the FMA pipe
+__device__ __forceinline__ uint32_t mad_hi_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// 1.0f if a > b or either is NaN (unordered), else 0.0f
+__device__ __forceinline__ float set_gt_f32(float a, float b) {
+  float d;
+  asm("set.gtu.f32.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
 }
 
 __device__ __forceinline__ float gumbel_from_word(uint32_t x) {
@@ -424,37 +439,51 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
               // of the Philox block with counter (v / 4, n, k, offset).  An
               // element can beat the running best only if g > best - adj/tau
               // - margin, i.e. 1 - u < 1 - exp(-A) <= A with
-              // A = exp(adj/tau - best + margin).  1 - u is exact from the
-              // inverted word, so the test costs one ex2 and no logarithm;
-              // the (1 + 2^-10) factor and the margin cover every rounding
-              // and approximation error, so a skipped element could never
-              // have won.  Survivors get the exact key.  The chunk is taken
-              // 8 columns at a time in a rolled loop: the fully unrolled form
-              // does not fit the instruction cache.
+              // A = exp(adj/tau - best + margin).  It is skipped when
+              // u <= 1 - A, with u exact (the mantissa trick below) and
+              // 1 - A rounded down, so that a skip implies 1 - u >= A: the
+              // test costs one ex2 and no logarithm, and the (1 + 2^-10)
+              // factor and the margin cover every rounding and approximation
+              // error in A, so a skipped element could never have won.
+              // Survivors get the exact key.  The test runs on the FMA pipe
+              // (mad.hi for the mantissa, the candidate mask accumulated in
+              // fp32), leaving the integer pipe to Philox.  The chunk is
+              // taken SAMPLE_PW columns at a time in a rolled loop: the fully
+              // unrolled form does not fit the instruction cache.
               const float s1 = p.inv_tau * 1.4426950408889634f;
 #pragma unroll 1
-              for (int h = 0; h < 4; ++h) {
-                const int cb = col0 + h * 8;
-                uint32_t acc[8];
-                tmem_ld_32x32b_x8(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                      static_cast<uint32_t>(buf * BN + cb),
-                                  acc);
-                tmem_ld_wait(acc);
-                float v[8];
-                if constexpr (LDT == DSPARK_BF16) {
-                  const int chunk = c * 4 + h;
-                  const uint4 w = ld_shared_v4(box + ((chunk ^ (row & 7)) << 4));
-                  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+              for (int h = 0; h < 32 / SAMPLE_PW; ++h) {
+                const int cb = col0 + h * SAMPLE_PW;
+                uint32_t acc[SAMPLE_PW];
 #pragma unroll
-                  for (int t = 0; t < 4; ++t) {
-                    v[2 * t] = __uint_as_float(acc[2 * t]) + __uint_as_float(ww[t] << 16);
-                    v[2 * t + 1] = __uint_as_float(acc[2 * t + 1]) +
-                                   __uint_as_float(ww[t] & 0xFFFF0000u);
+                for (int g8 = 0; g8 < SAMPLE_PW / 8; ++g8) {
+                  uint32_t (&a8)[8] = *reinterpret_cast<uint32_t (*)[8]>(acc + 8 * g8);
+                  tmem_ld_32x32b_x8(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                        static_cast<uint32_t>(buf * BN + cb + 8 * g8),
+                                    a8);
+                }
+#pragma unroll
+                for (int g8 = 0; g8 < SAMPLE_PW / 8; ++g8)
+                  tmem_ld_wait(*reinterpret_cast<uint32_t (*)[8]>(acc + 8 * g8));
+                float v[SAMPLE_PW];
+                if constexpr (LDT == DSPARK_BF16) {
+#pragma unroll
+                  for (int g8 = 0; g8 < SAMPLE_PW / 8; ++g8) {
+                    const int chunk = c * 4 + h * (SAMPLE_PW / 8) + g8;
+                    const uint4 w = ld_shared_v4(box + ((chunk ^ (row & 7)) << 4));
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                      v[8 * g8 + 2 * t] =
+                          __uint_as_float(acc[8 * g8 + 2 * t]) + __uint_as_float(ww[t] << 16);
+                      v[8 * g8 + 2 * t + 1] = __uint_as_float(acc[8 * g8 + 2 * t + 1]) +
+                                              __uint_as_float(ww[t] & 0xFFFF0000u);
+                    }
                   }
                 } else {
 #pragma unroll
-                  for (int t = 0; t < 2; ++t) {
-                    const int chunk = 2 * h + t;
+                  for (int t = 0; t < SAMPLE_PW / 4; ++t) {
+                    const int chunk = (SAMPLE_PW / 4) * h + t;
                     const uint4 w = ld_shared_v4(box + ((chunk ^ (row & 7)) << 4));
                     v[4 * t + 0] = __uint_as_float(acc[4 * t + 0]) + __uint_as_float(w.x);
                     v[4 * t + 1] = __uint_as_float(acc[4 * t + 1]) + __uint_as_float(w.y);
@@ -463,18 +492,18 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                   }
                 }
                 const int vb = v_tile0 + cb;
-                if (vb + 8 > p.vocab) {
+                if (vb + SAMPLE_PW > p.vocab) {
 #pragma unroll
-                  for (int e = 0; e < 8; ++e)
+                  for (int e = 0; e < SAMPLE_PW; ++e)
                     if (vb + e >= p.vocab) v[e] = -INFINITY;
                 }
                 const bool none = best_key == 0u || best_val != best_val;
                 const float margin = 1e-4f * (1.0f + fabsf(best_val));
                 const float s0 = none ? INFINITY
                                       : (margin - best_val) * 1.4426950408889634f + 0x1p-10f;
-                uint32_t x[8];
+                uint32_t x[SAMPLE_PW];
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
+                for (int i = 0; i < SAMPLE_PW / 4; ++i) {
                   uint32_t w4[4] = {static_cast<uint32_t>(vb >> 2) + i,
                                     static_cast<uint32_t>(m), static_cast<uint32_t>(k),
                                     p.offset};
@@ -482,13 +511,20 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
 #pragma unroll
                   for (int j = 0; j < 4; ++j) x[4 * i + j] = w4[j];
                 }
-                uint32_t cand = 0u;
+                float cand_f = 0.0f;  // sum of 2^e over the candidates
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
+                for (int e = 0; e < SAMPLE_PW; ++e) {
                   const float A = ex2_approx(fmaf(v[e], s1, s0));
-                  const float w = __uint_as_float(0x3F800000u | (~x[e] >> 9)) - 0x1.fffffep-1f;
-                  cand |= (!(w >= A) ? 1u : 0u) << e;  // NaN adj or best: always
+                  // u = (2 (x >> 9) + 1) 2^-24: 1 + (x >> 9) 2^-23 minus
+                  // 1 - 2^-24, exact by Sterbenz's lemma
+                  const float u = __uint_as_float(mad_hi_u32(x[e], 1u << 23, 0x3F800000u)) -
+                                  0x1.fffffep-1f;
+                  // candidate unless u <= 1 - A (NaN A: always a candidate)
+                  cand_f = fmaf(set_gt_f32(u, __fsub_rd(1.0f, A)), static_cast<float>(1 << e),
+                                cand_f);
                 }
+                uint32_t cand =
+                    __float_as_uint(cand_f + 0x1p23f) & ((1u << SAMPLE_PW) - 1u);
                 // survivors, lowest column first, through one copy of the
                 // exact key (a few per thousand elements)
                 if (__any_sync(0xFFFFFFFFu, cand != 0u)) {
@@ -498,7 +534,7 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                     float ve = v[0];
                     uint32_t xe = x[0];
 #pragma unroll
-                    for (int t = 1; t < 8; ++t) {
+                    for (int t = 1; t < SAMPLE_PW; ++t) {
                       ve = e == t ? v[t] : ve;
                       xe = e == t ? x[t] : xe;
                     }

@@ -63,7 +63,7 @@ def _hooked(ws, on):
 
 
 def test_sampling_and_fused_projection_time_out_and_recover():
-    """The same hook on the probabilistic chain (16 epilogue warps, of which
+    """The same hook on the probabilistic chain (12 epilogue warps, of which
     only the first four wait at the barrier) and on the fused output
     projection: both report DSPARK_DEV_TIMEOUT, write no out-of-range token
     and leave the context usable."""
