@@ -128,6 +128,23 @@ def test_sizes(N, K):
     _both(conf, mask, cost, T, 0.0, oracle.FORCE_RUNNING_MAX)
 
 
+@pytest.mark.parametrize("N,K", [(2048, 8), (1024, 15), (16384, 1), (5, 32)])
+def test_cross_request_ties(N, K):
+    """Survivals from a handful of exactly repeated values across thousands
+    of requests, all-equal and all-zero confidences: the global order must
+    break every tie by slot id, as the oracle's stable sort does."""
+    rng = np.random.default_rng(N + 7 * K)
+    vals = np.array([1.0, 0.5, 0.25, 0.75, 0.0], np.float32)
+    conf = vals[rng.integers(0, 5, (N, K))]
+    conf[rng.uniform(size=(N, K)) < 0.5] = 1.0
+    mask = (rng.uniform(size=N) < 0.8).astype(np.uint8)
+    L = N * K + 50
+    cost = (100 + 0.01 * np.arange(L)).astype(np.float32)
+    _both(conf, mask, cost, 7, 0.0, oracle.FORCE_RUNNING_MAX)
+    _both(np.ones((N, K), np.float32), None, cost, 7)
+    _both(np.zeros((N, K), np.float32), mask, cost, 7)
+
+
 def test_tiny_survivals_exact_sums():
     """Survivals spanning hundreds of binary orders of magnitude."""
     rng = np.random.default_rng(8)
