@@ -376,7 +376,7 @@ __device__ __forceinline__ double f64_from_key(unsigned long long k) {
 // sequentially.  Only 16-bit slot ids move (between sidx and stmp); keys
 // stay indexed by slot.  n log2(n / K) steps in log2(NK / K) levels, against
 // n log2(n)^2 / 4 compare-exchanges in about log2(n)^2 / 2 stages for a
-// bitonic network.  On return sidx[0 .. NK) is the order and keys[0 .. NK)
+// sorting network.  On return sidx[0 .. NK) is the order and keys[0 .. NK)
 // the keys in that order.
 // ------------------------------------------------------------------------
 __device__ __forceinline__ bool prio_first(unsigned long long ka, uint32_t sa,
@@ -470,8 +470,8 @@ constexpr int kMaxChunk = (kMaxSlots + 1 + SEL_THREADS - 1) / SEL_THREADS + 1;
 // `outputs`, writes survival, sorted_slots, n_eligible and n_sampling.
 __device__ void survival_order(const SelectArgs &a, const float *conf,
                                const bool outputs, unsigned long long *keys,
-                               uint16_t *sidx, uint16_t *stmp, const int P2,
-                               int *sh_int, int &n_s, uint32_t &st) {
+                               uint16_t *sidx, uint16_t *stmp, int *sh_int, int &n_s,
+                               uint32_t &st) {
   const int tid = threadIdx.x;
   const int NT = blockDim.x;
   const int N = a.N, K = a.K, NK = N * K;
@@ -496,7 +496,6 @@ __device__ void survival_order(const SelectArgs &a, const float *conf,
                : 0ull;
     }
   }
-  for (int i = NK + tid; i < P2; i += NT) keys[i] = 0ull;
   n_s = block_reduce(my_ns, OpAddInt(), 0, sh_int);
   const int S = n_s * K;
 
@@ -512,11 +511,12 @@ __device__ void survival_order(const SelectArgs &a, const float *conf,
 }
 
 __global__ void __launch_bounds__(SEL_THREADS, 1)
-    select_kernel(const SelectArgs a, const uint32_t stages, const int P2) {
+    select_kernel(const SelectArgs a, const uint32_t stages, const int cap) {
   extern __shared__ __align__(16) uint8_t dsm[];
-  unsigned long long *keys = reinterpret_cast<unsigned long long *>(dsm);  // [P2+1]
-  uint16_t *sidx = reinterpret_cast<uint16_t *>(keys + P2 + 1);           // [P2]
-  uint16_t *stmp = sidx + P2;                                             // [P2]
+  // cap = N * K slots (0 without the survival stage)
+  unsigned long long *keys = reinterpret_cast<unsigned long long *>(dsm);  // [cap+1]
+  uint16_t *sidx = reinterpret_cast<uint16_t *>(keys + cap + 1);          // [cap]
+  uint16_t *stmp = sidx + cap;                                            // [cap]
   double *Pd = reinterpret_cast<double *>(keys);  // after the scan: P_{j+1}
   int *len_sm = reinterpret_cast<int *>(dsm);     // after the budget
 
@@ -540,8 +540,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   const bool stale = a.conf_size != nullptr && (stages & kStageSurvival) &&
                      (stages & kStageBudget) && (stages & kStageAllocate);
   if (stages & kStageSurvival) {
-    survival_order(a, stale ? a.conf_size : a.conf, !stale, keys, sidx, stmp, P2,
-                   sh_int, n_s, st);
+    survival_order(a, stale ? a.conf_size : a.conf, !stale, keys, sidx, stmp, sh_int,
+                   n_s, st);
     S = n_s * K;
 
     // exact prefix sums of the sorted survivals
@@ -709,7 +709,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     // them): order the current confidences for the allocation
     __syncthreads();
     int n_s2 = 0;
-    survival_order(a, a.conf, true, keys, sidx, stmp, P2, sh_int, n_s2, st);
+    survival_order(a, a.conf, true, keys, sidx, stmp, sh_int, n_s2, st);
     if (tid == 0) sh_B = min(sh_B, n_s2 * K);
     __syncthreads();
   }
@@ -807,13 +807,6 @@ __global__ void __launch_bounds__(256)
 static std::mutex g_sel_mu;
 static bool g_sel_attr[128];
 
-static int next_pow2(int x) {
-  int p = 1;
-  while (p < x) p <<= 1;
-  return p;
-}
-
-
 dspark_status select_launch(const SelectArgs &a, uint32_t stages,
                             cudaStream_t stream) {
   int dev = 0;
@@ -829,18 +822,18 @@ dspark_status select_launch(const SelectArgs &a, uint32_t stages,
     }
   }
   const int NK = a.N * a.K;
-  int P2 = 0;
+  int cap = 0;
   size_t dyn = 0;
   if (stages & kStageSurvival) {
-    P2 = next_pow2(NK < 64 ? 64 : NK);
-    dyn = static_cast<size_t>(P2 + 1) * 8 + static_cast<size_t>(P2) * 4;
+    cap = NK;  // keys by slot, then in order; two 16-bit slot arrays
+    dyn = static_cast<size_t>(cap + 1) * 8 + static_cast<size_t>(cap) * 4;
   }
   if (stages & kStageAllocate) {
     const size_t need = static_cast<size_t>(a.N) * 4;
     if (need > dyn) dyn = need;
   }
   dyn = (dyn + 15) & ~static_cast<size_t>(15);
-  select_kernel<<<1, SEL_THREADS, dyn, stream>>>(a, stages, P2);
+  select_kernel<<<1, SEL_THREADS, dyn, stream>>>(a, stages, cap);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }
