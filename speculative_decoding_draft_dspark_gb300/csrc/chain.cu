@@ -137,10 +137,8 @@ __device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], const PhiloxKeys
   }
 }
 
-// Gumbel noise from one 32-bit word: u = (2 (x >> 9) + 1) 2^-24 (exact: the
-// mantissa trick gives 1 + (x >> 9) 2^-23, and subtracting 1 - 2^-24 is exact
-// by Sterbenz's lemma), g = -ln(-ln u).  ln is the accurate logf, which keeps
-// its relative accuracy for u next to 1.
+// 2^x by the hardware approximation (the skip test's bound carries margin
+// for its error)
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -161,6 +159,10 @@ __device__ __forceinline__ float set_gt_f32(float a, float b) {
   return d;
 }
 
+// Gumbel noise from one 32-bit word: u = (2 (x >> 9) + 1) 2^-24 (exact: the
+// mantissa trick gives 1 + (x >> 9) 2^-23, and subtracting 1 - 2^-24 is exact
+// by Sterbenz's lemma), g = -ln(-ln u).  ln is the accurate logf, which keeps
+// its relative accuracy for u next to 1.
 __device__ __forceinline__ float gumbel_from_word(uint32_t x) {
   const float u = __uint_as_float(0x3F800000u | (x >> 9)) - 0x1.fffffep-1f;
   return -logf(-logf(u));
