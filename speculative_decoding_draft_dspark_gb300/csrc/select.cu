@@ -385,19 +385,24 @@ __device__ __forceinline__ bool prio_first(unsigned long long ka, uint32_t sa,
 }
 
 constexpr int kMaxPerThread = (kMaxSlots + SEL_THREADS - 1) / SEL_THREADS;
+// outputs per thread and merge level, at least: fewer, longer runs mean
+// fewer co-rank searches, which bound a level (random key reads)
+constexpr int kMergeMinOut = 4;
 
 __device__ void block_merge_runs(unsigned long long *keys, uint16_t *sidx,
                                  uint16_t *stmp, const int NK, const int K) {
   const int tid = threadIdx.x;
   const int NT = blockDim.x;
-  const int C = (NK + NT - 1) / NT;
+  const int C = (NK + NT - 1) / NT;  // final reorder: outputs per thread
   const int p0 = min(NK, tid * C), p1 = min(NK, p0 + C);
+  const int Cm = max(C, kMergeMinOut);  // merge levels: outputs per thread
+  const int m0 = min(NK, tid * Cm), m1 = min(NK, m0 + Cm);
   uint16_t *src = sidx, *dst = stmp;
   for (int i = tid; i < NK; i += NT) sidx[i] = static_cast<uint16_t>(i);
   __syncthreads();
   for (int L = K; L < NK; L <<= 1) {
-    int p = p0;
-    while (p < p1) {
+    int p = m0;
+    while (p < m1) {
       // the pair of runs [base, base + L) and [base + L, base + 2L) holding p
       const int base = p - p % (2 * L);
       const int a_len = min(L, NK - base);
@@ -422,7 +427,7 @@ __device__ void block_merge_runs(unsigned long long *keys, uint16_t *sidx,
       uint32_t xa = A[min(ia, a_len - 1)];
       uint32_t xb = b_len > 0 ? B[min(ib, b_len - 1)] : 0u;
       unsigned long long ka = keys[xa], kb = keys[xb];
-      const int stop = min(p1, b0 + b_len);
+      const int stop = min(m1, b0 + b_len);
       for (; p < stop; ++p) {
         const bool take_a = ia < a_len && (ib >= b_len || prio_first(ka, xa, kb, xb));
         dst[p] = static_cast<uint16_t>(take_a ? xa : xb);
