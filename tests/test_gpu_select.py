@@ -145,6 +145,27 @@ def test_cross_request_ties(N, K):
     _both(np.zeros((N, K), np.float32), mask, cost, 7)
 
 
+def test_random_shapes_and_ties():
+    """Random batch shapes (N*K up to 16384, K up to 32) with tie-heavy and
+    continuous confidences, random masks, T and flags: every output equals
+    the oracle's bit for bit."""
+    rng = np.random.default_rng(2027)
+    for case in range(24):
+        K = int(rng.integers(1, 33))
+        N = int(rng.integers(1, 16384 // K + 1))
+        if rng.uniform() < 0.5:
+            vals = np.array([1.0, 0.5, 0.25, 0.75, 0.0, 0.125], np.float32)
+            conf = vals[rng.integers(0, len(vals), (N, K))]
+        else:
+            conf = rng.uniform(0, 1, (N, K)).astype(np.float32) ** rng.uniform(0.2, 3.0)
+        mask = (rng.uniform(size=N) < rng.uniform(0.3, 1.0)).astype(np.uint8)
+        L = int(rng.integers(8, N * K + 64))
+        cost = (100 + rng.uniform(0, 2, L).cumsum()).astype(np.float32)
+        T = int(rng.integers(0, L))
+        flags = int(rng.choice([0, oracle.FORCE_RUNNING_MAX]))
+        _both(conf, mask, cost, T, 0.0, flags)
+
+
 def test_tiny_survivals_exact_sums():
     """Survivals spanning hundreds of binary orders of magnitude."""
     rng = np.random.default_rng(8)
