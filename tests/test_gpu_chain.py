@@ -147,3 +147,34 @@ def test_stress_sampled_rows_and_planted_ties():
         if r["tok"][0] in (c0, c1):
             assert r["tok"][0] == c0
             assert got[n, k] == c0
+
+
+def test_random_shapes():
+    """Random shapes with ragged batch, vocabulary and rank tails (vocabulary
+    a multiple of 8, rank a multiple of 16, as the boundary requires), both
+    logits dtypes and layouts, argmax and probabilistic drafting: tokens
+    follow the near-tie rule against the oracle."""
+    from gpu_harness import run_chain, check_chain
+    rng = np.random.default_rng(4242)
+    for case in range(12):
+        N = int(rng.integers(1, 400))
+        K = int(rng.integers(1, 9))
+        vocab = 8 * int(rng.integers(1, 1200))
+        rank = 16 * int(rng.integers(1, 17))
+        dtype = "bf16" if rng.uniform() < 0.7 else "f32"
+        layout = "nkv" if rng.uniform() < 0.7 else "knv"
+        x = rng.standard_normal((N, K, vocab), dtype=np.float32) * np.float32(rng.uniform(0.5, 4))
+        logits = workloads.f32_to_bf16_bits(x) if dtype == "bf16" else x
+        sd = np.float32(rng.uniform(0.01, 0.2))
+        U = workloads.f32_to_bf16_bits(rng.standard_normal((vocab, rank), dtype=np.float32) * sd)
+        V = workloads.f32_to_bf16_bits(rng.standard_normal((vocab, rank), dtype=np.float32) * sd)
+        last = rng.integers(0, vocab, N).astype(np.int32)
+        sample = None
+        if rng.uniform() < 0.3:
+            sample = dict(seed=int(rng.integers(0, 2**63)), offset=int(rng.integers(0, 2**31)),
+                          tau=float(rng.uniform(0.5, 2.0)))
+        got, score, st = run_chain(logits, dtype, U, V, last, layout=layout, sample=sample)
+        assert st == 0, case
+        assert got.min() >= 0 and got.max() < vocab, case
+        assert check_chain(got, score, logits, dtype, U, V, last, sample=sample) \
+            <= max(1, N * K // 50), case
