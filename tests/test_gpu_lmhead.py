@@ -124,3 +124,23 @@ def test_headline_full_size():
     assert got.min() >= 0 and got.max() < cfg.vocab
     rows = np.random.default_rng(5).choice(cfg.N, 8, replace=False)
     assert _check(got, score, x["h"], x["W"], fac["U"], fac["V"], last, rows=rows) <= 1
+
+
+def test_random_shapes():
+    """Random shapes (batch, positions, vocabulary a multiple of 8, d a
+    multiple of 64, rank a multiple of 16) and hidden-state layouts."""
+    rng = np.random.default_rng(515)
+    for case in range(6):
+        N = int(rng.integers(1, 300))
+        K = int(rng.integers(1, 7))
+        vocab = 8 * int(rng.integers(1, 700))
+        d = 64 * int(rng.integers(1, 9))
+        rank = 16 * int(rng.integers(1, 17))
+        layout = "nkv" if rng.uniform() < 0.6 else "knv"
+        pad = int(rng.choice([0, 8, 64]))
+        h, W, U, V, last = _inputs(N, K, vocab, d, rank, seed=1000 + case,
+                                   sd=float(rng.uniform(1.0, 3.0)))
+        got, score, st = _run(h, W, U, V, last, layout=layout, pad=pad)
+        assert st == 0, case
+        assert got.min() >= 0 and got.max() < vocab, case
+        assert _check(got, score, h, W, U, V, last) <= max(1, N * K // 100), case

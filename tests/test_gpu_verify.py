@@ -110,3 +110,29 @@ def test_nobody_sampling():
     cu = np.zeros_like(cu)
     tgt, acc, bon, st = _run(tl, "bf16", draft, ln, cu, mask, 1024)
     assert np.all(acc == -1) and np.all(bon == -1) and np.all(tgt == -7)
+
+
+def test_random_batches():
+    """Random batches: request count, draft length, vocabulary (a multiple of
+    8 for bf16, of 4 for fp32), sampling mask, per-request verify lengths
+    and planted matches; every output equals the oracle's bit for bit."""
+    rng = np.random.default_rng(77)
+    for case in range(10):
+        N = int(rng.integers(1, 200))
+        K = int(rng.integers(1, 33))
+        dtype = "bf16" if rng.uniform() < 0.7 else "f32"
+        vocab = (8 if dtype == "bf16" else 4) * int(rng.integers(1, 2000))
+        mask = (rng.uniform(size=N) < rng.uniform(0.2, 1.0)).astype(np.uint8)
+        ln = np.where(mask == 1, rng.integers(0, K + 1, N), 0).astype(np.int32)
+        cu = np.concatenate([[0], np.cumsum(ln)]).astype(np.int32)
+        draft = rng.integers(0, vocab, (N, K)).astype(np.int32)
+        rows = oracle.verify_rows(ln, mask)
+        R = int(rows[-1])
+        x = rng.standard_normal((max(R, 1), vocab), dtype=np.float32) * np.float32(2.0)
+        for n in range(N):
+            for j in range(int(ln[n])):
+                if rng.uniform() < 0.6:
+                    x[rows[n] + j, draft[n, j]] = x[rows[n] + j].max() + 1.0
+        tl = workloads.f32_to_bf16_bits(x) if dtype == "bf16" else x
+        _, st = _check(tl, dtype, draft, ln, cu, mask, vocab)
+        assert st == 0, case
