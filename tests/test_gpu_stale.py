@@ -90,3 +90,29 @@ def test_out_of_range_old_buffer_sets_status():
     cost = (10 + np.arange(80)).astype(np.float32)
     r = _both(old, conf, None, cost, 2)
     assert r["status"] & oracle.CONF_OOR
+
+
+def test_random_shapes_and_ties():
+    """Random batch shapes, masks, T and flags, with an older confidence
+    buffer that is either an independent draw or the current one with a
+    few entries changed (tie-heavy values in half the cases): every output
+    equals the oracle's bit for bit."""
+    rng = np.random.default_rng(31337)
+    vals = np.array([1.0, 0.5, 0.25, 0.75, 0.0, 0.125], np.float32)
+    for case in range(16):
+        K = int(rng.integers(1, 33))
+        N = int(rng.integers(1, 16384 // K + 1))
+        if rng.uniform() < 0.5:
+            conf = vals[rng.integers(0, len(vals), (N, K))]
+            old = vals[rng.integers(0, len(vals), (N, K))]
+        else:
+            conf = rng.uniform(0, 1, (N, K)).astype(np.float32) ** rng.uniform(0.2, 3.0)
+            old = conf.copy()
+            pick = rng.uniform(size=(N, K)) < 0.1
+            old[pick] = rng.uniform(0, 1, int(pick.sum())).astype(np.float32)
+        mask = (rng.uniform(size=N) < rng.uniform(0.3, 1.0)).astype(np.uint8)
+        L = int(rng.integers(8, N * K + 64))
+        cost = (100 + rng.uniform(0, 2, L).cumsum()).astype(np.float32)
+        T = int(rng.integers(0, L))
+        flags = int(rng.choice([0, oracle.FORCE_RUNNING_MAX]))
+        _both(old, conf, mask, cost, T, 0.0, flags)
