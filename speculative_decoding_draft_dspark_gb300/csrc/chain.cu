@@ -76,8 +76,10 @@ constexpr int EPI_SAMPLE = 12;
 constexpr int SAMPLE_PW = 16;  // columns per step of the sampling epilogue
 constexpr uint32_t TMEM_COLS = 512;  // two 256-column fp32 accumulators
 // bytes of V worth protecting in L2 across positions (measured on GB300:
-// protecting more than this lets the logits stream evict it anyway)
-constexpr double kL2KeepBytes = 40.0 * 1024 * 1024;
+// with a 128 MiB V, protecting 6 tenths is fastest for batches of 8 to 256
+// requests and neutral at 1024; 8 tenths or more and the logits stream
+// evicts it anyway; a V that fits in L2, 63 MiB, is best protected whole)
+constexpr double kL2KeepBytes = 80.0 * 1024 * 1024;
 
 static_assert(CHAIN_SMEM_BYTES <= 232448, "shared memory budget");
 
