@@ -366,18 +366,19 @@ __device__ __forceinline__ double f64_from_key(unsigned long long k) {
 }
 
 // ------------------------------------------------------------------------
-// global priority order (larger key first, then smaller slot) of NK slots
-// whose keys come as sorted runs of K: the slots of one request, because a
-// survival never increases along a request (s[k+1] = s[k] * c with
-// 0 <= c <= 1, and rounding is monotone) and equal keys keep slot order.
-// Level l merges neighbouring runs of K * 2^l (merge path): every thread
-// writes ceil(NK / blockDim) consecutive outputs, finding how many of them
-// come from the left run by a binary search (the co-rank) and then merging
-// sequentially.  Only 16-bit slot ids move (between sidx and stmp); keys
-// stay indexed by slot.  n log2(n / K) steps in log2(NK / K) levels, against
+// global priority order (larger key first, then smaller slot) of NK slots.
+// Each warp first sorts segments of 128 slots in registers (a bitonic
+// network, below); then level l merges neighbouring runs of 128 * 2^l
+// (merge path): every thread writes ceil(NK / blockDim), at least four,
+// consecutive outputs, finding how many of them come from the left run by a
+// binary search (the co-rank) and then merging sequentially.  Only 16-bit
+// slot ids move (between sidx and stmp); keys stay indexed by slot.
+// n log2(n / 128) merge steps in log2(NK / 128) levels, against
 // n log2(n)^2 / 4 compare-exchanges in about log2(n)^2 / 2 stages for a
-// sorting network.  On return sidx[0 .. NK) is the order and keys[0 .. NK)
-// the keys in that order.
+// sorting network over the whole array.  (The requests' own runs of K
+// arrive sorted, since a survival never increases along a request, but the
+// segments subsume them.)  On return sidx[0 .. NK) is the order and
+// keys[0 .. NK) the keys in that order.
 // ------------------------------------------------------------------------
 __device__ __forceinline__ bool prio_first(unsigned long long ka, uint32_t sa,
                                            unsigned long long kb, uint32_t sb) {
@@ -389,6 +390,79 @@ constexpr int kMaxPerThread = (kMaxSlots + SEL_THREADS - 1) / SEL_THREADS;
 // fewer co-rank searches, which bound a level (random key reads)
 constexpr int kMergeMinOut = 4;
 
+// Before the merge: each warp sorts segments of 32 * kSegPerLane slots in
+// registers with a bitonic network (lane l holds elements l * E .. l * E +
+// E - 1 of the segment; strides of E or more exchange with another lane by
+// shuffle, shorter ones inside the lane), so the merge starts from runs of
+// 32 * E instead of K.  Every segment is sorted in priority order (the
+// direction bit is taken from the index inside the segment); the slots past
+// NK of the last segment are sentinels (key 0, slot 0xFFFF) that sort last
+// and are not written back.
+constexpr int kSegPerLane = 4;
+constexpr int kSegLen = 32 * kSegPerLane;
+// the network costs n log2(seg)^2 / 4 instructions' worth of exchanges: it
+// pays for small batches only; larger ones merge the requests' runs of K
+constexpr int kWarpSortMaxNK = 4096;
+
+__device__ void warp_sort_segments(const unsigned long long *keys, uint16_t *sidx,
+                                   const int NK) {
+  constexpr int E = kSegPerLane;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  for (int base = warp * kSegLen; base < NK; base += nwarps * kSegLen) {
+    unsigned long long k[E];
+    uint32_t v[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      const int i = base + lane * E + j;
+      k[j] = i < NK ? keys[i] : 0ull;
+      v[j] = i < NK ? static_cast<uint32_t>(i) : 0xFFFFu;
+    }
+#pragma unroll
+    for (int s = 2; s <= kSegLen; s <<= 1) {
+#pragma unroll
+      for (int d = s >> 1; d >= E; d >>= 1) {  // partner in another lane
+        const int m = d / E;
+        const bool lower = (lane & m) == 0;
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+          const int i = lane * E + j;
+          const unsigned long long pk = __shfl_xor_sync(0xFFFFFFFFu, k[j], m);
+          const uint32_t pv = __shfl_xor_sync(0xFFFFFFFFu, v[j], m);
+          if ((lower == ((i & s) == 0)) != prio_first(k[j], v[j], pk, pv)) {
+            k[j] = pk;
+            v[j] = pv;
+          }
+        }
+      }
+#pragma unroll
+      for (int dd = E / 2; dd >= 1; dd >>= 1) {  // partner in this lane
+        if (dd >= s) continue;
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+          if (j & dd) continue;
+          const int jj = j | dd;
+          const bool up = ((lane * E + j) & s) == 0;
+          if (up != prio_first(k[j], v[j], k[jj], v[jj])) {
+            const unsigned long long tk = k[j];
+            const uint32_t tv = v[j];
+            k[j] = k[jj];
+            v[j] = v[jj];
+            k[jj] = tk;
+            v[jj] = tv;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      const int i = base + lane * E + j;
+      if (i < NK) sidx[i] = static_cast<uint16_t>(v[j]);
+    }
+  }
+}
+
 __device__ void block_merge_runs(unsigned long long *keys, uint16_t *sidx,
                                  uint16_t *stmp, const int NK, const int K) {
   const int tid = threadIdx.x;
@@ -398,9 +472,15 @@ __device__ void block_merge_runs(unsigned long long *keys, uint16_t *sidx,
   const int Cm = max(C, kMergeMinOut);  // merge levels: outputs per thread
   const int m0 = min(NK, tid * Cm), m1 = min(NK, m0 + Cm);
   uint16_t *src = sidx, *dst = stmp;
-  for (int i = tid; i < NK; i += NT) sidx[i] = static_cast<uint16_t>(i);
+  const bool segments = NK <= kWarpSortMaxNK;
+  __syncthreads();  // the keys are in place
+  if (segments) {
+    warp_sort_segments(keys, sidx, NK);
+  } else {
+    for (int i = tid; i < NK; i += NT) sidx[i] = static_cast<uint16_t>(i);
+  }
   __syncthreads();
-  for (int L = K; L < NK; L <<= 1) {
+  for (int L = segments ? kSegLen : K; L < NK; L <<= 1) {
     int p = m0;
     while (p < m1) {
       // the pair of runs [base, base + L) and [base + L, base + 2L) holding p
