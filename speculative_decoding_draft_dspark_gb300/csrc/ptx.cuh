@@ -1,7 +1,7 @@
 // Inline-PTX wrappers for sm_103a: mbarrier, TMA (cp.async.bulk.tensor),
-// tcgen05 (TMEM allocation, MMA, commit, loads, fences), programmatic
-// dependent launch and the global timer.  Written from the PTX ISA's
-// instruction descriptions; no library code is used.
+// tcgen05 (TMEM allocation, MMA, commit, loads, fences) and the global
+// timer.  Written from the PTX ISA's instruction descriptions; no library
+// code is used.
 #pragma once
 
 #include <cstdint>
@@ -278,19 +278,6 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
-}
-
-// barrier among `count` threads of the CTA (ids 1..15; 0 is __syncthreads)
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// ------------------------------------------- programmatic dependent launch
-__device__ __forceinline__ void pdl_wait_primary() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ------------------------------------------------------------ float max
