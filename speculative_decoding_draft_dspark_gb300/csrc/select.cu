@@ -556,7 +556,7 @@ constexpr int kMaxChunk = (kMaxSlots + 1 + SEL_THREADS - 1) / SEL_THREADS + 1;
 __device__ void survival_order(const SelectArgs &a, const float *conf,
                                const bool outputs, unsigned long long *keys,
                                uint16_t *sidx, uint16_t *stmp, int *sh_int, int &n_s,
-                               uint32_t &st) {
+                               uint32_t &st, const int T_pf) {
   const int tid = threadIdx.x;
   const int NT = blockDim.x;
   const int N = a.N, K = a.K, NK = N * K;
@@ -583,6 +583,13 @@ __device__ void survival_order(const SelectArgs &a, const float *conf,
   }
   n_s = block_reduce(my_ns, OpAddInt(), 0, sh_int);
   const int S = n_s * K;
+  // the budget's cost slice into L1 (one 128-byte line per thread) while the
+  // order is built
+  if (T_pf >= 0 && T_pf < a.L) {
+    const int hi = min(a.L, T_pf + S + 1);
+    const int line = (T_pf >> 5) + tid;  // 32 floats per line
+    if (line * 32 < hi) asm volatile("prefetch.global.L1 [%0];" ::"l"(a.cost + line * 32));
+  }
 
   block_merge_runs(keys, sidx, stmp, NK, K);
   if (outputs) {
@@ -619,6 +626,10 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   int S = 0, n_s = 0;
   uint32_t st = 0;
 
+  // The budget reads cost[T .. T + b_max]: T is loaded now and the slice
+  // pulled into L1 before the order phase (see survival_order)
+  const int T_pf = (stages & kStageBudget) && (stages & kStageSurvival) ? *a.T_dev : -1;
+
   // ---------------------------------------------------- survival + order
   // Stale sizing: the budget comes from a.conf_size, then survival and order
   // are rebuilt from a.conf for the allocation.
@@ -626,7 +637,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
                      (stages & kStageBudget) && (stages & kStageAllocate);
   if (stages & kStageSurvival) {
     survival_order(a, stale ? a.conf_size : a.conf, !stale, keys, sidx, stmp, sh_int,
-                   n_s, st);
+                   n_s, st, T_pf);
     S = n_s * K;
 
     // exact prefix sums of the sorted survivals
@@ -732,8 +743,10 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
         fast = fast && den32 >= 1.17549435e-38f && isfinite(fa[i]);
         if (i < b1 - b0) amax = fmaxf(amax, fa[i]);
       }
-      fast = block_reduce(fast ? 1 : 0, OpMinInt(), 1, sh_int) != 0;
-      if (fast) amax = block_reduce(amax, OpMaxNan(), -INFINITY, sh_f);
+      // one reduction for both: a thread that cannot take the fp32 filter
+      // contributes NaN, which the maximum propagates to every thread
+      amax = block_reduce(fast ? amax : NAN, OpMaxNan(), -INFINITY, sh_f);
+      fast = !(amax != amax);
       const float thr = amax - amax * 1e-4f;
       unsigned long long best_k = 0ull;
       int best_b = INT_MAX;
@@ -794,7 +807,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     // them): order the current confidences for the allocation
     __syncthreads();
     int n_s2 = 0;
-    survival_order(a, a.conf, true, keys, sidx, stmp, sh_int, n_s2, st);
+    survival_order(a, a.conf, true, keys, sidx, stmp, sh_int, n_s2, st, -1);
     if (tid == 0) sh_B = min(sh_B, n_s2 * K);
     __syncthreads();
   }
