@@ -245,6 +245,21 @@ class Step:
         self.D.dspark_gather_verify_tokens(self.vi, self.B, self.draft, self.vt)
 
 
+def logits_desc(cfg):
+    """Element types of the chain's inputs, as the workload line names them."""
+    return ("bf16 logits/U/V" if cfg.logits_dtype == "bf16"
+            else f"{cfg.logits_dtype} logits, bf16 U/V")
+
+
+def cost_desc(cfg):
+    """The step-cost table's recipe, as the workload line names it."""
+    if cfg.cost_kind == "stepped":
+        return f"cost table L={cfg.L} stepped to {cfg.cost_cap}"
+    if cfg.cost_kind == "noisy":
+        return f"cost table L={cfg.L} noisy, forced monotone"
+    return f"cost table L={cfg.L} {cfg.cost_kind}"
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -390,9 +405,9 @@ def run_gpu(args):
                 "pages' workloads)",
         "config": {
             "workload": f"{cfg.name}: batch {cfg.N}, K {cfg.K}, vocab "
-                        f"{cfg.vocab}, rank {cfg.rank}, bf16 logits/U/V, "
+                        f"{cfg.vocab}, rank {cfg.rank}, {logits_desc(cfg)}, "
                         f"{cfg.n_nonsampling} chunked-prefill requests, T={cfg.T}, "
-                        f"cost table L={cfg.L} stepped to 4096",
+                        f"{cost_desc(cfg)}",
             "timing": ("CUDA graphs replayed; " + ("scheduler after the chain "
                        "on one stream" if serial else "scheduler on a second "
                        "stream alongside the chain, verify-token gather after "
