@@ -46,6 +46,17 @@ def test_w2_cost_index():
     assert r["B"] == g["expected"]["B"]
 
 
+def test_w4_draft_cost():
+    """The drafter cost on the device: fp32 constant in every denominator,
+    B = 2 through an exact tie of f(2) and f(3) (first index wins)."""
+    with open(os.path.join(GOLD, "w4_draft_cost.json")) as f:
+        g = json.load(f)
+    r = _both(np.array(g["conf"], np.float32), np.array(g["mask"], np.uint8),
+              np.array(g["cost"], np.float32), g["T"], g["draft_cost"])
+    assert r["B"] == g["expected"]["B"]
+    assert r["objective"] == g["expected"]["objective"]
+
+
 @pytest.mark.parametrize("name", list(workloads.CONFIGS))
 def test_workload(name):
     cfg = workloads.get_config(name)

@@ -114,3 +114,56 @@ def test_w3_stale_sizing():
     assert cur["draft_len"].tolist() == g["if_sized_from_current"]["draft_len"]
     old = oracle.select_step(conf_size, mask, cost, g["T"])
     assert old["draft_len"].tolist() == g["if_allocated_by_old_order"]["draft_len"]
+
+
+def test_w4_draft_cost():
+    """The drafter's cost is one fp32 constant added to every candidate
+    budget's step cost ("Adaptive Verification in vLLM", *The cost model*:
+    the verification and drafter tables are summed).  W4 is built so that
+    this reading gives B = 2 through an exact tie of f(2) and f(3)."""
+    g = _load("w4_draft_cost.json")
+    conf = np.array(g["conf"], np.float32)
+    mask = np.array(g["mask"], np.uint8)
+    cost = np.array(g["cost"], np.float32)
+    np.testing.assert_array_equal(cost.astype(np.float64), np.array(g["cost"]))
+    r = oracle.select_step(conf, mask, cost, g["T"], draft_cost=g["draft_cost"])
+    e = g["expected"]
+    assert r["B"] == e["B"]
+    np.testing.assert_array_equal(r["f"], np.array(e["f"]))
+    assert r["objective"] == e["objective"]
+    assert r["draft_len"].tolist() == e["draft_len"]
+    assert r["cu_len"].tolist() == e["cu_len"]
+    assert r["verify_idx"].tolist() == e["verify_idx"]
+    # the drafter cost matters: without it the budget differs
+    r0 = oracle.select_step(conf, mask, cost, g["T"], draft_cost=0.0)
+    assert r0["B"] == g["wrong_readings_B"]["no_draft_cost"]
+
+
+def test_w4_mistakes_would_change_b():
+    """Each wrong reading of the drafter cost gives another B on W4, computed
+    here in exact rationals (independent of the oracle's float path)."""
+    from fractions import Fraction as Fr
+    g = _load("w4_draft_cost.json")
+    T = g["T"]
+    cost = [Fr(c) for c in g["cost"]]
+    s = [Fr(1), Fr(1), Fr(3, 4)]
+    P = [Fr(0), s[0], s[0] + s[1], s[0] + s[1] + s[2]]
+    c32 = Fr(11744051, 1 << 24)
+    assert float(c32) == float(np.float32(g["draft_cost"]))
+
+    def first_argmax(f):
+        return f.index(max(f))
+
+    def B(num, den):
+        return first_argmax([num(b) / den(b) for b in range(4)])
+
+    n = lambda b: 1 + P[b]  # noqa: E731
+    assert B(n, lambda b: cost[T + b] + c32) == g["expected"]["B"]
+    w = g["wrong_readings_B"]
+    assert B(n, lambda b: cost[T + b]) == w["no_draft_cost"]
+    assert B(lambda b: n(b) + c32, lambda b: cost[T + b]) == w["in_numerator"]
+    assert B(n, lambda b: cost[T + b] + (c32 if b == 0 else 0)) == w["added_once_to_b0"]
+    assert B(n, lambda b: cost[T + b] + b * c32) == w["per_drafted_token"]
+    assert B(n, lambda b: cost[T + b] + Fr(g["draft_cost"])) == w["kept_in_fp64"]
+    for v in w.values():
+        assert v != g["expected"]["B"]
