@@ -179,26 +179,30 @@ DSPARK_API dspark_status dspark_chain_lmhead(
 /* ------------------------------------------------------------------------
  * dspark_chain_draft for callers that cannot allocate device memory.  The
  * pages have no counterpart: this is an interface convenience, not part of
- * the method.  Code running inside a CUDA graph capture, serving engines
- * that reserve the whole device memory at start-up and allow no later
- * allocation, and plugins running under a host runtime that owns every
- * allocation cannot hand out the chain workspace; this call takes its
- * scratch from a fixed array in the library's own device memory instead,
- * and allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ * the method.  Serving engines that reserve the whole device memory at
+ * start-up and allow no later allocation, plugins running under a host
+ * runtime that owns every allocation, and latency-critical code where
+ * cudaMalloc (which may synchronise the device) is not permitted cannot hand
+ * out the chain workspace; this call takes its scratch from a fixed array in
+ * the library's own device memory instead, and allocates nothing (no
+ * cudaMalloc, cudaFree or allocating library call).
  *
  * Arguments and results are those of dspark_chain_draft, without the
  * workspace.  device_status: optional device pointer to a uint32 that
  * receives this call's DSPARK_DEV_* bits (overwritten, not ORed); NULL to
  * discard them.
  * Limit: 256 + N*K*8 + K*ceil(N/128)*4 <= 262144 bytes of scratch (N = 1024,
- * K = 15 fits); larger sizes return DSPARK_ERR_UNSUPPORTED before anything
- * runs.  The scratch array (256 KiB) stays allocated on every GPU that
- * loaded the library until the process exits.  The first call on each
- * device looks up the array's device address with cudaGetSymbolAddress
- * (that device must be current); make that first call before any stream
- * capture.  Every call shares the one array and keeps the last call's
- * contents (each call clears what must start at zero), so calls that
- * overlap on the GPU race: order them on one stream or with events.
+ * K = 15 fits); larger sizes return DSPARK_ERR_UNSUPPORTED.  Every argument
+ * check (those of dspark_chain_draft and this limit) runs before the first
+ * CUDA call, so a rejected call enqueues nothing.  The scratch array
+ * (256 KiB) stays allocated on every GPU that loaded the library until the
+ * process exits.  The first call on each device looks up the array's device
+ * address with cudaGetSymbolAddress (that device must be current), and so
+ * does the first call after the device's context was replaced (for example
+ * by cudaDeviceReset); make that first call before any stream capture.
+ * Every call shares the one array and keeps the last call's contents (each
+ * call clears what must start at zero), so calls that overlap on the GPU
+ * race: order them on one stream or with events.
  * ------------------------------------------------------------------------ */
 DSPARK_API dspark_status dspark_chain_draft_noalloc(
     const void *logits, int32_t logits_dtype,

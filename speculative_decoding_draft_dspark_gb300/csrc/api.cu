@@ -42,12 +42,13 @@ static dspark_status check_ws(const void *ws, size_t bytes, size_t need) {
   return DSPARK_OK;
 }
 
-static dspark_status fill_chain_args(
-    ChainArgs &a, const void *logits, int32_t logits_dtype,
-    int64_t logits_stride_n, int64_t logits_stride_k, const void *U,
-    const void *V, const int32_t *last_token, int32_t N, int32_t K,
-    int32_t vocab, int32_t rank, int32_t *draft_tokens, float *draft_score,
-    void *workspace, size_t workspace_bytes) {
+dspark_status check_chain_inputs(const void *logits, int32_t logits_dtype,
+                                 int64_t logits_stride_n,
+                                 int64_t logits_stride_k, const void *U,
+                                 const void *V, const int32_t *last_token,
+                                 int32_t N, int32_t K, int32_t vocab,
+                                 int32_t rank, const int32_t *draft_tokens,
+                                 const float *draft_score) {
   if (!logits || !U || !V || !last_token || !draft_tokens)
     return DSPARK_ERR_INVALID_ARG;
   if (logits_dtype != DSPARK_BF16 && logits_dtype != DSPARK_F32)
@@ -67,8 +68,20 @@ static dspark_status fill_chain_args(
   if (!aligned(last_token, 4) || !aligned(draft_tokens, 4) ||
       (draft_score && !aligned(draft_score, 4)))
     return DSPARK_ERR_INVALID_ARG;
-  dspark_status s =
-      check_ws(workspace, workspace_bytes, chain_workspace_bytes(N, K));
+  return DSPARK_OK;
+}
+
+static dspark_status fill_chain_args(
+    ChainArgs &a, const void *logits, int32_t logits_dtype,
+    int64_t logits_stride_n, int64_t logits_stride_k, const void *U,
+    const void *V, const int32_t *last_token, int32_t N, int32_t K,
+    int32_t vocab, int32_t rank, int32_t *draft_tokens, float *draft_score,
+    void *workspace, size_t workspace_bytes) {
+  dspark_status s = check_chain_inputs(
+      logits, logits_dtype, logits_stride_n, logits_stride_k, U, V,
+      last_token, N, K, vocab, rank, draft_tokens, draft_score);
+  if (s != DSPARK_OK) return s;
+  s = check_ws(workspace, workspace_bytes, chain_workspace_bytes(N, K));
   if (s != DSPARK_OK) return s;
   a.logits = logits;
   a.logits_dtype = logits_dtype;

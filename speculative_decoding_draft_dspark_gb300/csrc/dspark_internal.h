@@ -42,6 +42,15 @@ struct ChainArgs {
   float inv_tau = 1.0f;
 };
 size_t chain_workspace_bytes(int32_t N, int32_t K);
+// Every host check of dspark_chain_draft except the workspace's (pointers,
+// dtype, sizes, strides, alignment); touches no CUDA state.
+dspark_status check_chain_inputs(const void *logits, int32_t logits_dtype,
+                                 int64_t logits_stride_n,
+                                 int64_t logits_stride_k, const void *U,
+                                 const void *V, const int32_t *last_token,
+                                 int32_t N, int32_t K, int32_t vocab,
+                                 int32_t rank, const int32_t *draft_tokens,
+                                 const float *draft_score);
 
 struct LmheadArgs {
   const void *h;  // bf16 [N, K, d] (strides in elements)

@@ -165,3 +165,34 @@ def test_product_path_never_touches_the_oracle():
                 src = open(os.path.join(root, fn)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle", src, re.M), fn
                 assert "oracle/" not in src, fn
+
+
+def _noalloc(lib, **kw):
+    a = dict(logits=FAKE, dt=0, sn=7 * 1024, sk=1024, U=FAKE, V=FAKE,
+             last=FAKE, N=4, K=7, vocab=1024, rank=16, draft=FAKE, score=None,
+             status=None, stream=None)
+    a.update(kw)
+    return lib.dspark_chain_draft_noalloc(
+        a["logits"], a["dt"], a["sn"], a["sk"], a["U"], a["V"], a["last"],
+        a["N"], a["K"], a["vocab"], a["rank"], a["draft"], a["score"],
+        a["status"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(logits=None), D.ERR_INVALID_ARG),
+    (dict(last=None), D.ERR_INVALID_ARG),
+    (dict(dt=7), D.ERR_INVALID_ARG),
+    (dict(N=0), D.ERR_INVALID_ARG),
+    (dict(K=33), D.ERR_UNSUPPORTED),
+    (dict(rank=24), D.ERR_UNSUPPORTED),
+    (dict(sk=1000), D.ERR_INVALID_ARG),
+    (dict(V=FAKE + 8), D.ERR_INVALID_ARG),
+    # 4096 x 8 slots need about 262 KB of scratch, over the 256 KiB array
+    (dict(N=4096, K=8, sn=8 * 1024), D.ERR_UNSUPPORTED),
+])
+def test_noalloc_checks_before_any_cuda_call(lib, kw, code):
+    """Every check of the no-allocation entry point runs before its first
+    CUDA call, so a rejected call enqueues nothing.  Without a GPU any CUDA
+    call would fail with DSPARK_ERR_CUDA, so the argument error itself shows
+    the order; with one, the call returns before touching the stream."""
+    assert _noalloc(lib, **kw) == code
