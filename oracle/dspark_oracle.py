@@ -120,10 +120,11 @@ def draft_uniforms(seed: int, offset: int, n: int, k: int, vocab: int) -> np.nda
     (low, high 32 bits of seed), keeping its top 23 bits: u = (2 * (x >> 9) +
     1) / 2^24, an odd multiple of 2^-24 that fp32 and fp64 both hold exactly.
     """
-    v = np.arange(vocab, dtype=np.uint64)
-    words = philox4x32_10(v >> np.uint64(2), n, k, offset,
+    blocks = np.arange((vocab + 3) // 4, dtype=np.uint64)  # counter word 0
+    words = philox4x32_10(blocks, n, k, offset,
                           seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)
-    x = np.choose((v & np.uint64(3)).astype(np.int64), words)
+    # entry v takes word v % 4 of block v // 4
+    x = np.stack(words, axis=1).reshape(-1)[:vocab]
     return (2.0 * (x >> np.uint64(9)).astype(np.float64) + 1.0) * 2.0 ** -24
 
 

@@ -26,3 +26,16 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    # near-tie divergences of the full-size chain parity tests: device tokens
+    # that differ from the oracle's only where the oracle's top-2 margin is
+    # below 1e-3 * |max|
+    h = sys.modules.get("gpu_harness")
+    log = getattr(h, "NEAR_TIE_LOG", None) if h else None
+    if not log:
+        return
+    terminalreporter.write_line("near-tie divergences (case: count / rows x positions checked):")
+    for case, near, checked in log:
+        terminalreporter.write_line(f"  {case}: {near} / {checked}")

@@ -21,6 +21,14 @@ DEV = "cuda:0"
 NEAR_TIE = 1e-3
 SCORE_RTOL = 1e-5
 
+# (case, near-tie divergences, rows x positions checked), printed at the end
+# of the run by the terminal-summary hook in conftest.py
+NEAR_TIE_LOG: list = []
+
+
+def report_near(case: str, near: int, checked: int) -> None:
+    NEAR_TIE_LOG.append((case, int(near), int(checked)))
+
 
 def up(a) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)

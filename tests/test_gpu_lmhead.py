@@ -7,7 +7,7 @@ and runs the same chain; the device accumulates bf16 products in fp32 over
 d + rank terms, so tokens follow the chain's near-tie rule and scores agree
 to 1e-5 relative.  Shapes span several tiles with ragged batch, vocabulary
 and rank tails, both hidden-state layouts, and the full headline size
-(sampled rows).
+(every row).
 """
 import numpy as np
 import pytest
@@ -122,8 +122,10 @@ def test_headline_full_size():
     got, score, st = _run(x["h"], x["W"], fac["U"], fac["V"], last)
     assert st == 0
     assert got.min() >= 0 and got.max() < cfg.vocab
-    rows = np.random.default_rng(5).choice(cfg.N, 8, replace=False)
-    assert _check(got, score, x["h"], x["W"], fac["U"], fac["V"], last, rows=rows) <= 1
+    from gpu_harness import report_near
+    near = _check(got, score, x["h"], x["W"], fac["U"], fac["V"], last)
+    report_near("lmhead headline (d 2048)", near, cfg.N * cfg.K)
+    assert near <= max(1, cfg.N * cfg.K // 100)
 
 
 def test_random_shapes():

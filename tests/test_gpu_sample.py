@@ -180,7 +180,8 @@ def test_full_size_workloads(name):
                                sample=SM)
     assert st == 0
     assert got.min() >= 0 and got.max() < cfg.vocab
-    rows = np.random.default_rng(4).choice(cfg.N, 24, replace=False)
+    from gpu_harness import report_near
     near = check_chain(got, score, logits, cfg.logits_dtype, fac["U"], fac["V"],
-                       last, rows=rows, sample=SM)
-    assert near <= 3
+                       last, sample=SM)
+    report_near(f"sample {name}", near, cfg.N * cfg.K)
+    assert near <= max(1, cfg.N * cfg.K // 100)
