@@ -55,6 +55,10 @@ def parse_args():
     ap.add_argument("--serial", action="store_true",
                     help="run the scheduler after the chain on one stream "
                          "instead of alongside it")
+    ap.add_argument("--link", action="store_true",
+                    help="measure the host-to-device link alone (pinned copies "
+                         "on 1/2/4/8 streams, and a kernel reading mapped pinned "
+                         "memory), the bound of the e2e number")
     return ap.parse_args()
 
 
@@ -824,8 +828,125 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------ host link (e2e bound)
+_LINK_PROBE = r"""
+// Host-to-device link probe: pinned copies on S streams, and SMs reading
+// mapped pinned memory directly.  Times with CUDA events; returns -1 on error.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+__global__ void read_mapped(const uint4 *__restrict__ src, size_t n,
+                            uint4 *__restrict__ sink) {
+  const size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  uint4 acc = make_uint4(0u, 0u, 0u, 0u);
+  for (size_t i = t; i < n; i += stride) {
+    const uint4 v = src[i];
+    acc.x ^= v.x; acc.y ^= v.y; acc.z ^= v.z; acc.w ^= v.w;
+  }
+  sink[t] = acc;
+}
+
+static void *g_host = nullptr, *g_dev = nullptr, *g_sink = nullptr;
+
+extern "C" int link_setup(size_t bytes) {
+  if (cudaHostAlloc(&g_host, bytes, cudaHostAllocMapped) != cudaSuccess) return -1;
+  if (cudaMalloc(&g_dev, bytes) != cudaSuccess) return -1;
+  if (cudaMalloc(&g_sink, 1024 * 1024 * 16) != cudaSuccess) return -1;
+  unsigned char *h = (unsigned char *)g_host;
+  for (size_t i = 0; i < bytes; i += 4096) h[i] = (unsigned char)i;
+  return 0;
+}
+
+extern "C" float link_copy_ms(size_t bytes, int streams) {
+  cudaStream_t st[16];
+  cudaEvent_t e0, e1, done[16];
+  if (streams < 1 || streams > 16) return -1.0f;
+  cudaEventCreate(&e0); cudaEventCreate(&e1);
+  for (int s = 0; s < streams; ++s) {
+    cudaStreamCreateWithFlags(&st[s], cudaStreamNonBlocking);
+    cudaEventCreateWithFlags(&done[s], cudaEventDisableTiming);
+  }
+  cudaEventRecord(e0, st[0]);
+  for (int s = 1; s < streams; ++s) cudaStreamWaitEvent(st[s], e0, 0);
+  const size_t part = (bytes / streams) & ~(size_t)4095;
+  for (int s = 0; s < streams; ++s) {
+    const size_t off = part * s, n = s == streams - 1 ? bytes - off : part;
+    cudaMemcpyAsync((char *)g_dev + off, (const char *)g_host + off, n,
+                    cudaMemcpyHostToDevice, st[s]);
+    cudaEventRecord(done[s], st[s]);
+  }
+  for (int s = 1; s < streams; ++s) cudaStreamWaitEvent(st[0], done[s], 0);
+  cudaEventRecord(e1, st[0]);
+  float ms = -1.0f;
+  if (cudaEventSynchronize(e1) == cudaSuccess) cudaEventElapsedTime(&ms, e0, e1);
+  for (int s = 0; s < streams; ++s) { cudaStreamDestroy(st[s]); cudaEventDestroy(done[s]); }
+  cudaEventDestroy(e0); cudaEventDestroy(e1);
+  return cudaGetLastError() == cudaSuccess ? ms : -1.0f;
+}
+
+extern "C" float link_mapped_ms(size_t bytes, int blocks) {
+  void *dptr = nullptr;
+  if (cudaHostGetDevicePointer(&dptr, g_host, 0) != cudaSuccess) return -1.0f;
+  if (blocks < 1 || (size_t)blocks * 256 * 16 > 1024 * 1024 * 16) return -1.0f;
+  cudaEvent_t e0, e1;
+  cudaEventCreate(&e0); cudaEventCreate(&e1);
+  cudaEventRecord(e0, 0);
+  read_mapped<<<blocks, 256>>>((const uint4 *)dptr, bytes / 16, (uint4 *)g_sink);
+  cudaEventRecord(e1, 0);
+  float ms = -1.0f;
+  if (cudaEventSynchronize(e1) == cudaSuccess) cudaEventElapsedTime(&ms, e0, e1);
+  cudaEventDestroy(e0); cudaEventDestroy(e1);
+  return cudaGetLastError() == cudaSuccess ? ms : -1.0f;
+}
+"""
+
+
+def run_link(args):
+    """The host-to-device link alone, for the bytes one headline step copies
+    (the logits, 939.5 MB): pinned copies split over 1/2/4/8 streams, and
+    SMs reading the mapped pinned buffer themselves.  Best of 5 each."""
+    import ctypes
+    import tempfile
+    import workloads
+    cfg = workloads.get_config(args.workload)
+    nbytes = cfg.N * cfg.K * cfg.vocab * (2 if cfg.logits_dtype == "bf16" else 4)
+    tmp = tempfile.mkdtemp(prefix="dspark_link_")
+    src, lib = os.path.join(tmp, "link.cu"), os.path.join(tmp, "link.so")
+    with open(src, "w") as f:
+        f.write(_LINK_PROBE)
+    subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a",
+                           "-O3", "-shared", "-Xcompiler", "-fPIC", "-o", lib, src])
+    L = ctypes.CDLL(lib)
+    L.link_setup.argtypes = [ctypes.c_size_t]
+    L.link_copy_ms.argtypes = [ctypes.c_size_t, ctypes.c_int]
+    L.link_copy_ms.restype = ctypes.c_float
+    L.link_mapped_ms.argtypes = [ctypes.c_size_t, ctypes.c_int]
+    L.link_mapped_ms.restype = ctypes.c_float
+    assert L.link_setup(nbytes) == 0
+    out = {"metric": "host-to-device bytes per second for one step's inputs",
+           "bytes": nbytes, "workload": workload_desc(cfg), "copies": {},
+           "mapped_read": {}}
+    for streams in (1, 2, 4, 8):
+        L.link_copy_ms(nbytes, streams)  # warm-up
+        ms = min(L.link_copy_ms(nbytes, streams) for _ in range(5))
+        assert ms > 0
+        out["copies"][f"{streams}_streams"] = {"ms": round(ms, 3),
+                                               "GB_s": round(nbytes / ms / 1e6, 1)}
+    for blocks in (152, 304, 608, 1024):
+        L.link_mapped_ms(nbytes, blocks)
+        ms = min(L.link_mapped_ms(nbytes, blocks) for _ in range(5))
+        assert ms > 0
+        out["mapped_read"][f"{blocks}_blocks"] = {"ms": round(ms, 3),
+                                                  "GB_s": round(nbytes / ms / 1e6, 1)}
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.link:
+        run_link(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
