@@ -55,6 +55,11 @@ def parse_args():
     ap.add_argument("--serial", action="store_true",
                     help="run the scheduler after the chain on one stream "
                          "instead of alongside it")
+    ap.add_argument("--l2", action="store_true",
+                    help="measure how much of a V-sized buffer L2 keeps between "
+                         "re-reads while a logits-sized stream passes through (the "
+                         "chain's access pattern without its compute); run under "
+                         "ncu with dram__bytes_read.sum for the DRAM bytes")
     ap.add_argument("--link", action="store_true",
                     help="measure the host-to-device link alone (pinned copies "
                          "on 1/2/4/8 streams, and a kernel reading mapped pinned "
@@ -902,22 +907,152 @@ extern "C" float link_mapped_ms(size_t bytes, int blocks) {
 """
 
 
+_L2_PROBE = r"""
+// The chain's L2 access pattern without its compute: every sweep (one draft
+// position) re-reads a buffer R (the Markov factor V) split into one slice
+// per pair of CTAs (the two request tiles of a vocabulary group, which run
+// on one TPC), alternating direction, with a fractional evict_last policy,
+// and streams a fresh chunk of a buffer S (the position's logits) once with
+// evict_first.  DRAM bytes come from ncu; the kernel returns nothing useful.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+__device__ __forceinline__ uint4 ld_hint(const uint4 *p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+
+__global__ void chain_pattern(const uint4 *__restrict__ R, size_t r_n,
+                              const uint4 *__restrict__ S, size_t s_n,
+                              int sweeps, float keep, uint4 *__restrict__ sink) {
+  uint64_t pk, pf;
+  asm volatile("createpolicy.fractional.L2::evict_last.L2::evict_first.b64 %0, %1;"
+               : "=l"(pk) : "f"(keep));
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pf));
+  const size_t groups = gridDim.x / 2, g = blockIdx.x / 2;
+  const size_t lo = r_n * g / groups, hi = r_n * (g + 1) / groups;
+  const size_t chunk = s_n / ((size_t)sweeps * gridDim.x);
+  uint4 acc = make_uint4(0u, 0u, 0u, 0u);
+  const size_t nt = blockDim.x;
+  for (int w = 0; w < sweeps; ++w) {
+    // four independent loads in flight per thread and step
+    for (size_t t0 = 0; t0 < hi - lo; t0 += 4 * nt) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const size_t t = t0 + u * nt + threadIdx.x;
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (t < hi - lo) v[u] = ld_hint(R + ((w & 1) ? hi - 1 - t : lo + t), pk);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc.x ^= v[u].x; acc.y ^= v[u].y; acc.z ^= v[u].z; acc.w ^= v[u].w;
+      }
+    }
+    const size_t c0 = ((size_t)w * gridDim.x + blockIdx.x) * chunk;
+    for (size_t t0 = 0; t0 < chunk; t0 += 4 * nt) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const size_t t = t0 + u * nt + threadIdx.x;
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (t < chunk) v[u] = ld_hint(S + c0 + t, pf);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc.x ^= v[u].x; acc.y ^= v[u].y; acc.z ^= v[u].z; acc.w ^= v[u].w;
+      }
+    }
+  }
+  sink[blockIdx.x * blockDim.x + threadIdx.x] = acc;
+}
+
+static uint4 *g_R = nullptr, *g_S = nullptr, *g_sink = nullptr;
+
+extern "C" int l2_setup(size_t r_bytes, size_t s_bytes) {
+  if (cudaMalloc(&g_R, r_bytes) != cudaSuccess) return -1;
+  if (cudaMalloc(&g_S, s_bytes) != cudaSuccess) return -1;
+  if (cudaMalloc(&g_sink, 4 << 20) != cudaSuccess) return -1;
+  cudaMemset(g_R, 1, r_bytes);
+  cudaMemset(g_S, 2, s_bytes);
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -1;
+}
+
+extern "C" float l2_run_ms(size_t r_bytes, size_t s_bytes, int sweeps, float keep,
+                           int blocks) {
+  if (blocks < 2 || blocks * 512 * 16 > (4 << 20)) return -1.0f;
+  cudaEvent_t e0, e1;
+  cudaEventCreate(&e0); cudaEventCreate(&e1);
+  cudaEventRecord(e0, 0);
+  chain_pattern<<<blocks, 512>>>(g_R, r_bytes / 16, g_S, s_bytes / 16, sweeps,
+                                 keep, g_sink);
+  cudaEventRecord(e1, 0);
+  float ms = -1.0f;
+  if (cudaEventSynchronize(e1) == cudaSuccess) cudaEventElapsedTime(&ms, e0, e1);
+  cudaEventDestroy(e0); cudaEventDestroy(e1);
+  return cudaGetLastError() == cudaSuccess ? ms : -1.0f;
+}
+"""
+
+
+def _build_probe(src_text, name):
+    import ctypes
+    import tempfile
+    tmp = tempfile.mkdtemp(prefix="dspark_probe_")
+    src, lib = os.path.join(tmp, name + ".cu"), os.path.join(tmp, name + ".so")
+    with open(src, "w") as f:
+        f.write(src_text)
+    subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a",
+                           "-O3", "-shared", "-Xcompiler", "-fPIC", "-o", lib, src])
+    return ctypes.CDLL(lib)
+
+
+def run_l2(args):
+    """The chain's L2 pattern alone (see _L2_PROBE), at the headline's sizes:
+    a re-read buffer of 48 MB .. V (134.2 MB) kept with 0.4 .. 1.0 of its
+    lines evict_last, and the K = 7 positions' logits (939.5 MB) streamed
+    once.  One launch per line of the table, in the printed order; the DRAM
+    bytes of each launch come from ncu (one pass: dram__bytes_read.sum)."""
+    import ctypes
+    import workloads
+    cfg = workloads.get_config(args.workload)
+    v_bytes = cfg.vocab * cfg.rank * 2
+    s_bytes = cfg.N * cfg.K * cfg.vocab * 2
+    L = _build_probe(_L2_PROBE, "l2")
+    L.l2_setup.argtypes = [ctypes.c_size_t, ctypes.c_size_t]
+    L.l2_run_ms.argtypes = [ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int,
+                            ctypes.c_float, ctypes.c_int]
+    L.l2_run_ms.restype = ctypes.c_float
+    assert L.l2_setup(v_bytes, s_bytes) == 0
+    blocks = 150
+    L.l2_run_ms(v_bytes, s_bytes, cfg.K, 0.6, blocks)  # warm-up (not a table line)
+    rows = []
+    for mb in (48, 64, 80, 96, 112, v_bytes / 2**20):
+        r = (int(mb * 2**20) // (16 * 150)) * 16 * 150
+        for keep in (0.4, 0.6, 0.8, 1.0):
+            assert L.l2_run_ms(r, s_bytes, cfg.K, keep, blocks) > 0
+            rows.append({"reread_MB": round(r / 1e6, 1), "keep": keep,
+                         "algorithmic_if_all_rereads_hit_MB":
+                             round((r + s_bytes) / 1e6, 1),
+                         "if_no_reread_hits_MB":
+                             round((cfg.K * r + s_bytes) / 1e6, 1)})
+    print(json.dumps({"probe": "chain L2 pattern", "workload": workload_desc(cfg),
+                      "sweeps": cfg.K, "stream_MB": round(s_bytes / 1e6, 1),
+                      "blocks": blocks, "launches_after_warmup": rows}), flush=True)
+
+
 def run_link(args):
     """The host-to-device link alone, for the bytes one headline step copies
     (the logits, 939.5 MB): pinned copies split over 1/2/4/8 streams, and
     SMs reading the mapped pinned buffer themselves.  Best of 5 each."""
     import ctypes
-    import tempfile
     import workloads
     cfg = workloads.get_config(args.workload)
     nbytes = cfg.N * cfg.K * cfg.vocab * (2 if cfg.logits_dtype == "bf16" else 4)
-    tmp = tempfile.mkdtemp(prefix="dspark_link_")
-    src, lib = os.path.join(tmp, "link.cu"), os.path.join(tmp, "link.so")
-    with open(src, "w") as f:
-        f.write(_LINK_PROBE)
-    subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a",
-                           "-O3", "-shared", "-Xcompiler", "-fPIC", "-o", lib, src])
-    L = ctypes.CDLL(lib)
+    L = _build_probe(_LINK_PROBE, "link")
     L.link_setup.argtypes = [ctypes.c_size_t]
     L.link_copy_ms.argtypes = [ctypes.c_size_t, ctypes.c_int]
     L.link_copy_ms.restype = ctypes.c_float
@@ -946,6 +1081,9 @@ def main():
     args = parse_args()
     if args.link:
         run_link(args)
+        return
+    if args.l2:
+        run_l2(args)
         return
     if args.impl == "reference":
         run_reference(args)
