@@ -12,11 +12,17 @@
 //
 // Numerics: survivals are fp64 products taken left to right (each one IEEE
 // multiply), sort keys are their bit patterns, and P_b is the exact sum of
-// the first b survivals rounded once, computed as a 256-bit fixed-point
-// prefix scan (integer addition is associative, so the parallel scan gives
-// the same bits as any order).  f(b) is then one fp64 add and one fp64
-// divide.  B is therefore decided on exactly the values the definition
-// names.
+// the first b survivals rounded once, computed as a fixed-point prefix scan
+// (integer addition is associative, so the parallel scan gives the same
+// bits as any order): 128 bits wide when every nonzero survival lies within
+// 2^61 of the largest (all terms exact), 256 bits otherwise.  f(b) is then
+// one fp64 add and one fp64 divide.  B is therefore decided on exactly the
+// values the definition names.
+//
+// The order: up to 4096 slots, 64-bit composites (the survival's fp64 bits
+// truncated to 50, then the slot id) sorted per warp in registers and merged
+// (merge path), with a check that sends ties of the truncated key to the
+// exact path; larger batches, and that case, merge the fp64 keys by slot.
 //
 // The kernel runs the stages requested by a mask, so the fused call and the
 // four separate calls share one implementation.
@@ -163,6 +169,86 @@ __device__ __forceinline__ double from_fixed(const Acc256 &a, int e_max) {
 }
 
 // ------------------------------------------------------------------------
+// 128-bit form of the same fixed point, for when every nonzero term lies
+// within 2^-kFixG128 of the largest: the largest term occupies bits
+// [kFixG128, kFixG128 + 53), every term is an exact integer (no sticky
+// bit), and a sum of up to 2^14 terms stays below bit 128.  The sums are
+// then exact and one rounding gives the same double as the 256-bit form.
+// ------------------------------------------------------------------------
+constexpr int kFixG128 = 61;
+
+struct Acc128 {
+  unsigned long long lo, hi;
+};
+
+__device__ __forceinline__ void acc128_add(Acc128 &a, const Acc128 &b) {
+  asm("add.cc.u64 %0, %0, %2;\n\t"
+      "addc.u64 %1, %1, %3;"
+      : "+l"(a.lo), "+l"(a.hi)
+      : "l"(b.lo), "l"(b.hi));
+}
+
+// s * 2^-u, u = e_max - 1075 - kFixG128; requires the biased exponent of s
+// (1 for subnormals) >= e_max - kFixG128
+__device__ __forceinline__ Acc128 to_fixed128(double s, int e_max) {
+  const unsigned long long bits =
+      static_cast<unsigned long long>(__double_as_longlong(s));
+  int ex = static_cast<int>((bits >> 52) & 0x7FF);
+  unsigned long long m = bits & 0xFFFFFFFFFFFFFull;
+  if (ex == 0)
+    ex = 1;
+  else
+    m |= 1ull << 52;
+  const int shift = ex - e_max + kFixG128;  // 0 .. kFixG128
+  Acc128 r;
+  r.lo = m << shift;
+  r.hi = shift == 0 ? 0ull : m >> (64 - shift);
+  return r;
+}
+
+// a * 2^u rounded to the nearest double, ties to even
+__device__ __forceinline__ double from_fixed128(const Acc128 &a, int e_max) {
+  int h;
+  if (a.hi)
+    h = 64 + 63 - __clzll(static_cast<long long>(a.hi));
+  else if (a.lo)
+    h = 63 - __clzll(static_cast<long long>(a.lo));
+  else
+    return 0.0;
+  const int u = e_max - 1075 - kFixG128;
+  int rb = h - 52;
+  const int rb_sub = -1074 - u;
+  if (rb < rb_sub) rb = rb_sub;
+  // the whole value fits (a < 2^53): exact.  (Not reached from the scan,
+  // whose nonzero sums have their top bit at kFixG128 + 52 or above.)
+  if (rb <= 0) return ldexp(static_cast<double>(a.lo), u);
+  unsigned long long mant =
+      rb >= 64 ? a.hi >> (rb - 64) : (a.lo >> rb) | (a.hi << (64 - rb));
+  mant &= (1ull << 53) - 1ull;
+  const int pos = rb - 1;  // the round bit
+  bool round, sticky;
+  if (pos >= 64) {
+    round = (a.hi >> (pos - 64)) & 1ull;
+    sticky = a.lo != 0ull || (a.hi & ((1ull << (pos - 64)) - 1ull)) != 0ull;
+  } else {
+    round = (a.lo >> pos) & 1ull;
+    sticky = pos > 0 && (a.lo & ((1ull << pos) - 1ull)) != 0ull;
+  }
+  if (round && (sticky || (mant & 1ull))) mant += 1ull;
+  int e2 = rb + u;
+  if (mant == (1ull << 53)) {
+    mant >>= 1;
+    e2 += 1;
+  }
+  const unsigned long long bits =
+      mant >= (1ull << 52)
+          ? (static_cast<unsigned long long>(e2 + 52 + 1023) << 52) |
+                (mant & ((1ull << 52) - 1ull))
+          : mant;  // subnormal, e2 == -1074
+  return __longlong_as_double(static_cast<long long>(bits));
+}
+
+// ------------------------------------------------------------------------
 // block-level scans and reductions (blockDim = SEL_THREADS)
 // ------------------------------------------------------------------------
 __device__ __forceinline__ int shfl_up(int v, int o) { return __shfl_up_sync(FULL, v, o); }
@@ -175,6 +261,13 @@ __device__ __forceinline__ Acc256 shfl_up(const Acc256 &v, int o) {
   r.w2 = __shfl_up_sync(FULL, v.w2, o);
   r.w3 = __shfl_up_sync(FULL, v.w3, o);
   r.sticky = __shfl_up_sync(FULL, v.sticky, o);
+  return r;
+}
+
+__device__ __forceinline__ Acc128 shfl_up(const Acc128 &v, int o) {
+  Acc128 r;
+  r.lo = __shfl_up_sync(FULL, v.lo, o);
+  r.hi = __shfl_up_sync(FULL, v.hi, o);
   return r;
 }
 
@@ -197,6 +290,13 @@ struct OpMinNan {
 struct OpAcc {
   __device__ Acc256 operator()(Acc256 a, const Acc256 &b) const {
     acc_add(a, b);
+    return a;
+  }
+};
+
+struct OpAcc128 {
+  __device__ Acc128 operator()(Acc128 a, const Acc128 &b) const {
+    acc128_add(a, b);
     return a;
   }
 };
@@ -546,6 +646,182 @@ __device__ void block_merge_runs(unsigned long long *keys, uint16_t *sidx,
 }
 
 // ------------------------------------------------------------------------
+// Fast order for up to kFastMaxNK slots, on one 64-bit composite per slot:
+// the top 50 bits of the survival's fp64 pattern (sign 0, exponent, 38
+// mantissa bits), subtracted from their largest value, then the 14-bit
+// slot; non-sampling slots get a key part above every survival.  Ascending
+// composites are survival descending, slot ascending, and every comparison
+// is one 64-bit compare of one shared-memory word.  Each warp first sorts
+// segments of 128 composites in registers (a bitonic network over
+// shuffles), then merge levels (merge path, as above) combine the runs.
+// Truncating the bit pattern is monotone, so the result is the fp64 order
+// wherever neighbours differ in those 50 bits; two neighbours equal there
+// but different in fp64 (within 2^-38 of each other) are detected
+// afterwards and send the whole order to the fp64 merge above.
+// ------------------------------------------------------------------------
+constexpr int kFastMaxNK = 4096;
+constexpr int kCompSlotBits = 14;  // slot ids below 16384
+constexpr int kCompDrop = 14;      // fp64 bits dropped from the key part
+// key part of survival 0 (bits 0) is kCompTop; of 1.0, kCompTop - (1.0's
+// bits >> kCompDrop); the key part of non-sampling slots is kCompTop + 1
+constexpr unsigned long long kCompTop = 0x3FF0000000000000ull >> kCompDrop;
+constexpr unsigned long long kCompNonSampling = (kCompTop + 1ull) << kCompSlotBits;
+static_assert(kFastMaxNK <= (1 << kCompSlotBits), "slot ids fit the composite");
+static_assert(((kCompTop + 1ull) << kCompSlotBits) < ~0ull - (1ull << kCompSlotBits),
+              "composites stay below the padding value");
+constexpr int kCompSegPerLane = 4;
+constexpr int kCompSegLen = 32 * kCompSegPerLane;
+
+// ascending bitonic sort of the warp's 32 * E composites (lane l holds
+// elements l * E .. l * E + E - 1); fully unrolled (a rolled form with
+// runtime stage and distance loops measured slower)
+template <int E>
+__device__ __forceinline__ void warp_bitonic_composite(unsigned long long (&v)[E]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 2; s <= 32 * E; s <<= 1) {
+#pragma unroll
+    for (int d = s >> 1; d >= E; d >>= 1) {  // partner in another lane
+      const int m = d / E;
+      const bool lower = (lane & m) == 0;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const unsigned long long o = __shfl_xor_sync(FULL, v[e], m);
+        const bool up = ((lane * E + e) & s) == 0;
+        v[e] = (lower == up) ? (o < v[e] ? o : v[e]) : (o > v[e] ? o : v[e]);
+      }
+    }
+#pragma unroll
+    for (int dd = E / 2; dd >= 1; dd >>= 1) {  // partner in this lane
+      if (dd >= s) continue;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if (e & dd) continue;
+        const int ee = e | dd;
+        const bool up = ((lane * E + e) & s) == 0;
+        const unsigned long long x = v[e], y = v[ee];
+        const bool sw = up ? (x > y) : (x < y);
+        v[e] = sw ? y : x;
+        v[ee] = sw ? x : y;
+      }
+    }
+  }
+}
+
+// Orders keys[0 .. NK) (fp64 survival bits + 1 by slot, 0 for non-sampling)
+// with the composites; ca, cb hold NK composites each.  Returns false, with
+// keys and sidx untouched, if two eligible neighbours tie in fp32 but differ
+// in fp64.
+__device__ bool fast_order(unsigned long long *keys, uint16_t *sidx,
+                           unsigned long long *ca, unsigned long long *cb,
+                           const int NK, const int S) {
+  constexpr int E = kCompSegPerLane;
+  const int tid = threadIdx.x;
+  const int NT = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nwarps = NT >> 5;
+  // composites, sorted per 128-slot segment
+  for (int base = warp * kCompSegLen; base < NK; base += nwarps * kCompSegLen) {
+    unsigned long long v[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int i = base + lane * E + e;
+      unsigned long long c = ~0ull;  // past NK: sorts last, not written
+      if (i < NK) {
+        const unsigned long long k = keys[i];
+        c = k == 0ull ? kCompNonSampling
+                      : ((kCompTop - ((k - 1ull) >> kCompDrop)) << kCompSlotBits);
+        c |= static_cast<unsigned long long>(i);
+      }
+      v[e] = c;
+    }
+    warp_bitonic_composite<E>(v);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int i = base + lane * E + e;
+      if (i < NK) ca[i] = v[e];
+    }
+  }
+  __syncthreads();
+  // merge levels: every thread writes Cm consecutive outputs of a pair of
+  // runs after finding its co-rank by binary search
+  const int Cm = max((NK + NT - 1) / NT, kMergeMinOut);
+  const int m0 = min(NK, tid * Cm), m1 = min(NK, m0 + Cm);
+  unsigned long long *src = ca, *dst = cb;
+  for (int L = kCompSegLen; L < NK; L <<= 1) {
+    int p = m0;
+    while (p < m1) {
+      const int base = p - p % (2 * L);
+      const int a_len = min(L, NK - base);
+      const int b0 = base + a_len;
+      const int b_len = min(L, NK - b0);
+      const unsigned long long *A = src + base;
+      const unsigned long long *B = src + b0;
+      const int q = p - base;
+      int lo = max(0, q - b_len), hi = min(q, a_len);
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (A[mid] < B[q - mid - 1])
+          lo = mid + 1;
+        else
+          hi = mid;
+      }
+      int ia = lo, ib = q - lo;
+      unsigned long long ka = ia < a_len ? A[ia] : ~0ull;
+      unsigned long long kb = ib < b_len ? B[ib] : ~0ull;
+      const int stop = min(m1, b0 + b_len);
+      for (; p < stop; ++p) {
+        const bool take_a = ka < kb;  // composites are distinct; ~0 = exhausted
+        dst[p] = take_a ? ka : kb;
+        if (take_a) {
+          ++ia;
+          ka = ia < a_len ? A[ia] : ~0ull;
+        } else {
+          ++ib;
+          kb = ib < b_len ? B[ib] : ~0ull;
+        }
+      }
+    }
+    __syncthreads();
+    unsigned long long *t = src;
+    src = dst;
+    dst = t;
+  }
+  // eligible neighbours with equal key parts must be equal in fp64
+  constexpr unsigned long long kSlotMask = (1ull << kCompSlotBits) - 1ull;
+  int bad = 0;
+  for (int j = tid; j + 1 < S; j += NT) {
+    const unsigned long long x = src[j], y = src[j + 1];
+    if ((x >> kCompSlotBits) == (y >> kCompSlotBits) &&
+        keys[x & kSlotMask] != keys[y & kSlotMask])
+      bad = 1;
+  }
+  if (__syncthreads_or(bad)) return false;
+  // slots and keys into sorted order (all reads before any write)
+  constexpr int kMaxOut = (kFastMaxNK + SEL_THREADS - 1) / SEL_THREADS;
+  unsigned long long kv[kMaxOut];
+  uint32_t sv[kMaxOut];
+#pragma unroll
+  for (int c = 0; c < kMaxOut; ++c) {
+    const int j = tid + c * NT;
+    if (j < NK) {
+      sv[c] = static_cast<uint32_t>(src[j] & kSlotMask);
+      kv[c] = keys[sv[c]];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int c = 0; c < kMaxOut; ++c) {
+    const int j = tid + c * NT;
+    if (j < NK) {
+      keys[j] = kv[c];
+      sidx[j] = static_cast<uint16_t>(sv[c]);
+    }
+  }
+  __syncthreads();
+  return true;
+}
+
+// ------------------------------------------------------------------------
 // the scheduler kernel
 // ------------------------------------------------------------------------
 constexpr int kMaxChunk = (kMaxSlots + 1 + SEL_THREADS - 1) / SEL_THREADS + 1;
@@ -555,30 +831,41 @@ constexpr int kMaxChunk = (kMaxSlots + 1 + SEL_THREADS - 1) / SEL_THREADS + 1;
 // `outputs`, writes survival, sorted_slots, n_eligible and n_sampling.
 __device__ void survival_order(const SelectArgs &a, const float *conf,
                                const bool outputs, unsigned long long *keys,
-                               uint16_t *sidx, uint16_t *stmp, int *sh_int, int &n_s,
+                               uint16_t *sidx, uint16_t *stmp,
+                               unsigned long long *sortbuf, int *sh_int, int &n_s,
                                uint32_t &st, const int T_pf) {
   const int tid = threadIdx.x;
   const int NT = blockDim.x;
   const int N = a.N, K = a.K, NK = N * K;
   int my_ns = 0;
+  constexpr int KG = 8;  // confidences loaded together (one memory round trip)
   for (int n = tid; n < N; n += NT) {
     const bool samp = a.mask == nullptr || a.mask[n] != 0;
     my_ns += samp ? 1 : 0;
+    const float *cn = conf + static_cast<size_t>(n) * K;
     double prod = 1.0;
-    for (int k = 0; k < K; ++k) {
-      float c = conf[static_cast<size_t>(n) * K + k];
-      if (!(c >= 0.0f && c <= 1.0f)) {
-        st |= DSPARK_DEV_CONF_OOR;
-        c = (c > 1.0f) ? 1.0f : 0.0f;  // NaN and negatives -> 0
+    for (int k0 = 0; k0 < K; k0 += KG) {
+      float cg[KG];
+#pragma unroll
+      for (int u = 0; u < KG; ++u) cg[u] = k0 + u < K ? cn[k0 + u] : 0.0f;
+#pragma unroll
+      for (int u = 0; u < KG; ++u) {
+        const int k = k0 + u;
+        if (k >= K) break;
+        float c = cg[u];
+        if (!(c >= 0.0f && c <= 1.0f)) {
+          st |= DSPARK_DEV_CONF_OOR;
+          c = (c > 1.0f) ? 1.0f : 0.0f;  // NaN and negatives -> 0
+        }
+        if (c == 0.0f) c = 0.0f;  // -0 -> +0: sort keys are bit patterns
+        prod = __dmul_rn(prod, static_cast<double>(c));
+        if (outputs && a.survival)
+          a.survival[static_cast<size_t>(n) * K + k] =
+              samp ? __double2float_rn(prod) : 0.0f;
+        keys[n * K + k] =
+            samp ? static_cast<unsigned long long>(__double_as_longlong(prod)) + 1ull
+                 : 0ull;
       }
-      if (c == 0.0f) c = 0.0f;  // -0 -> +0: sort keys are bit patterns
-      prod = __dmul_rn(prod, static_cast<double>(c));
-      if (outputs && a.survival)
-        a.survival[static_cast<size_t>(n) * K + k] =
-            samp ? __double2float_rn(prod) : 0.0f;
-      keys[n * K + k] =
-          samp ? static_cast<unsigned long long>(__double_as_longlong(prod)) + 1ull
-               : 0ull;
     }
   }
   n_s = block_reduce(my_ns, OpAddInt(), 0, sh_int);
@@ -591,7 +878,12 @@ __device__ void survival_order(const SelectArgs &a, const float *conf,
     if (line * 32 < hi) asm volatile("prefetch.global.L1 [%0];" ::"l"(a.cost + line * 32));
   }
 
-  block_merge_runs(keys, sidx, stmp, NK, K);
+  bool done = false;
+  if (NK <= kFastMaxNK) {
+    __syncthreads();  // keys by slot are in place
+    done = fast_order(keys, sidx, sortbuf, sortbuf + NK, NK, S);
+  }
+  if (!done) block_merge_runs(keys, sidx, stmp, NK, K);
   if (outputs) {
     if (a.sorted_slots)
       for (int j = tid; j < S; j += NT) a.sorted_slots[j] = sidx[j];
@@ -609,6 +901,9 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   unsigned long long *keys = reinterpret_cast<unsigned long long *>(dsm);  // [cap+1]
   uint16_t *sidx = reinterpret_cast<uint16_t *>(keys + cap + 1);          // [cap]
   uint16_t *stmp = sidx + cap;                                            // [cap]
+  // two composite arrays for the fast order: [2 * cap]
+  unsigned long long *sortbuf = reinterpret_cast<unsigned long long *>(
+      dsm + ((static_cast<size_t>(cap + 1) * 8 + static_cast<size_t>(cap) * 4 + 7) & ~static_cast<size_t>(7)));
   double *Pd = reinterpret_cast<double *>(keys);  // after the scan: P_{j+1}
   int *len_sm = reinterpret_cast<int *>(dsm);     // after the budget
 
@@ -636,8 +931,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
   const bool stale = a.conf_size != nullptr && (stages & kStageSurvival) &&
                      (stages & kStageBudget) && (stages & kStageAllocate);
   if (stages & kStageSurvival) {
-    survival_order(a, stale ? a.conf_size : a.conf, !stale, keys, sidx, stmp, sh_int,
-                   n_s, st, T_pf);
+    survival_order(a, stale ? a.conf_size : a.conf, !stale, keys, sidx, stmp, sortbuf,
+                   sh_int, n_s, st, T_pf);
     S = n_s * K;
 
     // exact prefix sums of the sorted survivals
@@ -648,15 +943,46 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     }
     const int C = (S + NT - 1) / NT;
     const int j0 = min(S, tid * C), j1 = min(S, j0 + C);
-    Acc256 tot = acc_zero();
-    for (int j = j0; j < j1; ++j) acc_add(tot, to_fixed(key_value(keys[j]), e_max));
-    Acc256 run = block_excl_scan(tot, OpAcc(), acc_zero(), sh_acc,
-                                 static_cast<Acc256 *>(nullptr));
-    for (int j = j0; j < j1; ++j) {
-      acc_add(run, to_fixed(key_value(keys[j]), e_max));
-      const double P = from_fixed(run, e_max);
-      Pd[j] = P;  // this thread's own element: no other thread reads it
-      if (a.prefix_sum) a.prefix_sum[j + 1] = P;
+    // the smallest nonzero survival: the sorted keys end with the zeros
+    // (key 1), so it sits just before the first of them (checked for the
+    // batches of the fast order only; larger ones span too many decades)
+    bool narrow = false;
+    if (S <= kFastMaxNK) {
+      if (tid == 0) sh_int[SEL_WARPS] = e_max;
+      __syncthreads();
+      for (int j = j0; j < j1; ++j) {
+        if (keys[j] != 1ull && (j + 1 == S || keys[j + 1] == 1ull)) {
+          const int ex = static_cast<int>(((keys[j] - 1ull) >> 52) & 0x7FF);
+          sh_int[SEL_WARPS] = ex == 0 ? 1 : ex;
+        }
+      }
+      __syncthreads();
+      narrow = sh_int[SEL_WARPS] >= e_max - kFixG128;
+      __syncthreads();
+    }
+    if (narrow) {
+      Acc128 tot = {0ull, 0ull};
+      for (int j = j0; j < j1; ++j) acc128_add(tot, to_fixed128(key_value(keys[j]), e_max));
+      Acc128 run = block_excl_scan(tot, OpAcc128(), Acc128{0ull, 0ull},
+                                   reinterpret_cast<Acc128 *>(sh_acc),
+                                   static_cast<Acc128 *>(nullptr));
+      for (int j = j0; j < j1; ++j) {
+        acc128_add(run, to_fixed128(key_value(keys[j]), e_max));
+        const double P = from_fixed128(run, e_max);
+        Pd[j] = P;  // this thread's own element: no other thread reads it
+        if (a.prefix_sum) a.prefix_sum[j + 1] = P;
+      }
+    } else {
+      Acc256 tot = acc_zero();
+      for (int j = j0; j < j1; ++j) acc_add(tot, to_fixed(key_value(keys[j]), e_max));
+      Acc256 run = block_excl_scan(tot, OpAcc(), acc_zero(), sh_acc,
+                                   static_cast<Acc256 *>(nullptr));
+      for (int j = j0; j < j1; ++j) {
+        acc_add(run, to_fixed(key_value(keys[j]), e_max));
+        const double P = from_fixed(run, e_max);
+        Pd[j] = P;  // this thread's own element: no other thread reads it
+        if (a.prefix_sum) a.prefix_sum[j + 1] = P;
+      }
     }
     if (tid == 0 && a.prefix_sum) a.prefix_sum[0] = 0.0;
     __syncthreads();
@@ -807,7 +1133,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     // them): order the current confidences for the allocation
     __syncthreads();
     int n_s2 = 0;
-    survival_order(a, a.conf, true, keys, sidx, stmp, sh_int, n_s2, st, -1);
+    survival_order(a, a.conf, true, keys, sidx, stmp, sortbuf, sh_int, n_s2, st, -1);
     if (tid == 0) sh_B = min(sh_B, n_s2 * K);
     __syncthreads();
   }
@@ -925,6 +1251,8 @@ dspark_status select_launch(const SelectArgs &a, uint32_t stages,
   if (stages & kStageSurvival) {
     cap = NK;  // keys by slot, then in order; two 16-bit slot arrays
     dyn = static_cast<size_t>(cap + 1) * 8 + static_cast<size_t>(cap) * 4;
+    if (NK <= kFastMaxNK)  // two composite arrays
+      dyn = ((dyn + 7) & ~static_cast<size_t>(7)) + static_cast<size_t>(NK) * 16;
   }
   if (stages & kStageAllocate) {
     const size_t need = static_cast<size_t>(a.N) * 4;

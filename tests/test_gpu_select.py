@@ -177,6 +177,28 @@ def test_random_shapes_and_ties():
         _both(conf, mask, cost, T, 0.0, flags)
 
 
+def test_survivals_equal_in_fp32_but_not_in_fp64():
+    """Survivals that differ in fp64 but round to the same fp32 value must
+    still be ordered by their fp64 values (then slot).  Request 1's second
+    survival, (1 - 2^-24)^2 = 1 - 2^-23 + 2^-48, rounds to the fp32 value of
+    request 0's survivals, 1 - 2^-23, yet is larger and has a larger slot id;
+    a larger random batch repeats the pattern with confidences a few ulps
+    below 1."""
+    a = np.float32(1.0 - 2.0 ** -23)
+    b = np.float32(1.0 - 2.0 ** -24)
+    conf = np.array([[a, 1.0], [b, b]], np.float32)
+    cost = (10.0 + 0.5 * np.arange(16)).astype(np.float32)
+    r = _both(conf, None, cost, 2)
+    assert r["order"].tolist() == [2, 3, 0, 1]
+    rng = np.random.default_rng(99)
+    for N, K in ((300, 6), (256, 7), (600, 6)):
+        ulps = rng.integers(0, 6, (N, K))
+        conf = (1.0 - ulps * 2.0 ** -24).astype(np.float32)
+        conf[rng.uniform(size=(N, K)) < 0.3] = np.float32(0.5)
+        cost = (10.0 + 0.5 * np.arange(N * K + 8)).astype(np.float32)
+        _both(conf, None, cost, N)
+
+
 def test_tiny_survivals_exact_sums():
     """Survivals spanning hundreds of binary orders of magnitude."""
     rng = np.random.default_rng(8)
