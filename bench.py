@@ -37,6 +37,7 @@ WORKLOAD = "headline"
 CHAIN_SRC = os.path.join(ROOT, "speculative_decoding_draft_dspark_gb300",
                          "csrc", "chain.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "chain_kernel_headline_ncu.md")
+SAMPLE_PROFILE = os.path.join(ROOT, "profiles", "chain_kernel_sample_headline_ncu.md")
 
 
 def parse_args():
@@ -117,20 +118,25 @@ def measured_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def recorded_traffic():
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
-    on the current chain kernel source (else None)."""
-    if not os.path.exists(TRAFFIC_FILE):
+def _recorded(path, field):
+    """A per-launch figure from a committed ncu summary, if the summary was
+    taken on the current chain kernel source (else None)."""
+    if not os.path.exists(path):
         return None
     src_hash = hashlib.sha256(open(CHAIN_SRC, "rb").read()).hexdigest()[:16]
-    bytes_ = None
+    value = None
     hash_ok = False
-    for line in open(TRAFFIC_FILE):
+    for line in open(path):
         if line.startswith("kernel_source_sha256_16:"):
             hash_ok = line.split(":", 1)[1].strip() == src_hash
-        if line.startswith("dram_bytes_per_launch:"):
-            bytes_ = float(line.split(":", 1)[1].strip())
-    return bytes_ if hash_ok else None
+        if line.startswith(field + ":"):
+            value = float(line.split(":", 1)[1].strip())
+    return value if hash_ok else None
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes of the argmax chain (ncu summary)."""
+    return _recorded(TRAFFIC_FILE, "dram_bytes_per_launch")
 
 
 class ClockSampler:
@@ -588,17 +594,23 @@ def run_sample_chain(st, cfg, stream, iters=50):
     elems = cfg.N * cfg.K * cfg.vocab
     out["elements"] = elems
     out["gelem_per_s"] = round(elems / (out["sample_us"] * 1e-6) / 1e9, 2)
-    # ALU roofline: per element, a quarter of a Philox4x32-10 block (10 rounds
-    # of 2 wide multiplies and 2 three-input XORs = 40 ops per 4 elements),
-    # the adjusted-logit add and the comparison: 12 integer / fp32 ops; peak
-    # = 128 such ops per SM per clock at the 2070 MHz maximum SM clock
+    # Issue roofline: the path is bound by instruction issue (Philox words,
+    # the skip test), so the work is the warp instructions one launch issues,
+    # measured by ncu (smsp__inst_executed.sum, recorded with the kernel
+    # source's hash), and the peak is four warp instructions per SM per clock
+    # at the 2070 MHz maximum SM clock
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    peak_tops = sms * 128 * 2.070e9 / 1e12
-    achieved = elems * 12 / (out["sample_us"] * 1e-6) / 1e12
-    out["roofline"] = {"bound": "alu", "ops_per_element": 12,
-                       "achieved": round(achieved, 2), "peak": round(peak_tops, 2),
-                       "unit": "Tops/s", "frac": round(achieved / peak_tops, 4),
-                       "peak_source": "derived: SMs x 128 lanes x 2070 MHz"}
+    peak = sms * 4 * 2.070e9 / 1e12
+    inst = (_recorded(SAMPLE_PROFILE, "warp_instructions_per_launch")
+            if cfg.name == "headline" else None)
+    achieved = None if inst is None else inst / (out["sample_us"] * 1e-6) / 1e12
+    out["roofline"] = {"bound": "issue", "achieved": None if achieved is None else round(achieved, 4),
+                       "peak": round(peak, 4), "unit": "T warp instructions/s",
+                       "frac": None if achieved is None else round(achieved / peak, 4),
+                       "warp_instructions_per_launch": inst,
+                       "thread_instructions_per_element":
+                           None if inst is None else round(inst * 32 / elems, 2),
+                       "peak_source": "derived: SMs x 4 issue slots x 2070 MHz"}
     out["note"] = ("dspark_chain_sample vs dspark_chain_draft, back-to-back "
                    "launches; not part of the step metric")
     return out

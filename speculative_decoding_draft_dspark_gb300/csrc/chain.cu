@@ -163,11 +163,13 @@ __device__ __forceinline__ float set_gt_f32(float a, float b) {
 
 // Gumbel noise from one 32-bit word: u = (2 (x >> 9) + 1) 2^-24 (exact: the
 // mantissa trick gives 1 + (x >> 9) 2^-23, and subtracting 1 - 2^-24 is exact
-// by Sterbenz's lemma), g = -ln(-ln u).  ln is the accurate logf, which keeps
-// its relative accuracy for u next to 1.
+// by Sterbenz's lemma), g = -ln(-ln u).  The inner ln is the accurate logf,
+// which keeps its relative accuracy for u next to 1 (the large g); its
+// result lies in [6e-8, 16.7], where the hardware log2 (absolute error near
+// 1e-6 in g) is accurate enough for the outer one.
 __device__ __forceinline__ float gumbel_from_word(uint32_t x) {
   const float u = __uint_as_float(0x3F800000u | (x >> 9)) - 0x1.fffffep-1f;
-  return -logf(-logf(u));
+  return -__logf(-logf(u));
 }
 
 template <int LDT, bool SAMPLE, int EPI>
@@ -417,6 +419,12 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
       uint32_t best_key = 0u;  // below every real key
       int best_idx = 0x7FFFFFFF;
       float best_val = -INFINITY;  // the value behind best_key (sampling)
+      // sampling: the row's best published so far by any thread of any CTA
+      // (read one piece ahead), a shared threshold for the skip test
+      uint32_t shared_key = 0u;
+      unsigned long long shared_pend = 0ull;
+      unsigned long long *row_slot =
+          row_ok ? &p.slots[static_cast<size_t>(k) * p.N + m] : nullptr;
       for (int i = 0; i < nt && ok; ++i, ++ig) {
         const TileGeom g = tile_geom(k, i, qb, qe);
         const int buf = ig & 1;
@@ -501,10 +509,6 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                   for (int e = 0; e < SAMPLE_PW; ++e)
                     if (vb + e >= p.vocab) v[e] = -INFINITY;
                 }
-                const bool none = best_key == 0u || best_val != best_val;
-                const float margin = 1e-4f * (1.0f + fabsf(best_val));
-                const float s0 = none ? INFINITY
-                                      : (margin - best_val) * 1.4426950408889634f + 0x1p-10f;
                 uint32_t x[SAMPLE_PW];
 #pragma unroll
                 for (int i = 0; i < SAMPLE_PW / 4; ++i) {
@@ -515,6 +519,28 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
 #pragma unroll
                   for (int j = 0; j < 4; ++j) x[4 * i + j] = w4[j];
                 }
+                // The skip test's threshold: this thread's best or the row's
+                // best published by any thread, whichever is larger.  Every
+                // published key is some element's exact key, so an element
+                // skipped against it (with the margin below) can neither be
+                // the row's winner nor tie with it.
+                shared_key = max(shared_key, static_cast<uint32_t>(shared_pend >> 32));
+                if (row_slot)
+                  shared_pend = *reinterpret_cast<volatile unsigned long long *>(row_slot);
+                if (best_key == 0u && shared_key == 0u) {
+                  // nothing to compare with yet: the piece's first element
+                  // seeds the threshold with its exact key
+                  const float key0 = fmaf(v[0], p.inv_tau, gumbel_from_word(x[0]));
+                  best_key = f32_key(key0);
+                  best_idx = vb;
+                  best_val = key0;
+                }
+                const uint32_t tkey = max(best_key, shared_key);
+                const float tval = tkey == best_key ? best_val : f32_from_key(tkey);
+                const bool none = tval != tval;
+                const float margin = 1e-4f * (1.0f + fabsf(tval));
+                const float s0 = none ? INFINITY
+                                      : (margin - tval) * 1.4426950408889634f + 0x1p-10f;
                 float cand_f = 0.0f;  // sum of 2^e over the candidates
 #pragma unroll
                 for (int e = 0; e < SAMPLE_PW; ++e) {
@@ -530,8 +556,10 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                 uint32_t cand =
                     __float_as_uint(cand_f + 0x1p23f) & ((1u << SAMPLE_PW) - 1u);
                 // survivors, lowest column first, through one copy of the
-                // exact key (a few per thousand elements)
+                // exact key (a few per thousand elements); an improvement is
+                // published at once so other threads can skip against it
                 if (__any_sync(0xFFFFFFFFu, cand != 0u)) {
+                  const uint32_t key_before = best_key;
                   while (cand != 0u) {
                     const int e = __ffs(cand) - 1;
                     cand &= cand - 1u;
@@ -551,6 +579,11 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                       best_val = key;
                     }
                   }
+                  if (best_key != key_before && row_slot)
+                    atomicMax(row_slot,
+                              (static_cast<unsigned long long>(best_key) << 32) |
+                                  static_cast<unsigned long long>(
+                                      0xFFFFFFFFu - static_cast<uint32_t>(best_idx)));
                 }
               }
             } else {
