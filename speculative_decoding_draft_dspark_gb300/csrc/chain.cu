@@ -40,7 +40,9 @@
 //               (TMEM lane quarter w % 4)
 //   warps 8-11  more epilogue warps on the same lane quarters (warp w takes
 //               quarter w % 4; the warps of a quarter split each tile's
-//               32-column chunks); sampling runs warps 8-15
+//               32-column chunks; they also decode the winners and, with a
+//               single tile per position, gather half of each U row);
+//               sampling runs warps 8-15
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
@@ -172,7 +174,10 @@ __device__ __forceinline__ float gumbel_from_word(uint32_t x) {
   return -__logf(-logf(u));
 }
 
-template <int LDT, bool SAMPLE, int EPI>
+// ONE_TILE: every CTA owns at most one tile per position (a small
+// vocabulary); the position boundary is then all there is, and A is gathered
+// by two sub-groups each loading half of every row (see the gather below)
+template <int LDT, bool SAMPLE, int EPI, bool ONE_TILE>
 __global__ void __launch_bounds__(chain_threads(EPI), 1)
     chain_kernel(const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmL,
@@ -222,7 +227,9 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], EPI);
     }
-    mbar_init(a_full, 4);  // the first four epilogue warps gather A
+    // the warps that gather A arrive: sub-group 0, and sub-group 1 too with
+    // a single tile per position
+    mbar_init(a_full, ONE_TILE ? 8 : 4);
     mbar_init(mma_done, 1);
     *abort_flag = 0u;
     fence_mbarrier_init();
@@ -375,7 +382,9 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
             raise_status(p.status, DSPARK_DEV_TOKEN_OOR);
           }
         }
-      } else if (sg == 0) {
+      } else if (sg == 0 || (ONE_TILE && sg == 1)) {
+        // (sub-group 1 needs the winners only when it gathers: one tile per
+        // position)
         if (!(ok = grid_wait(p, k - 1, m_tile, abort_flag, EPI))) break;
         if (row_ok) {
           const unsigned long long key = *reinterpret_cast<volatile unsigned long long *>(
@@ -390,27 +399,55 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
           }
         }
       }
-      // gather this position's U rows into A, one 512-byte row per warp
-      // instruction (lane j copies 16-byte chunk j of the row); the MMAs of
-      // position k-1 have all retired, their last accumulator was consumed
-      const int nchunk = sg == 0 ? KB * 8 : 0;
-      for (int r = 0; r < 32 && sg == 0; ++r) {
-        const int rp = __shfl_sync(0xFFFFFFFFu, prev, r);
-        const int rrow = q * 32 + r;
-        const bool rok = (m0 + rrow) < p.N;
-        if (lane < nchunk) {
-          const int kb = lane >> 3, c = lane & 7;
-          const uint32_t dst = a_base + kb * A_KBLOCK_BYTES + rrow * 128 +
-                               ((c ^ (rrow & 7)) << 4);
-          if (rok && lane * 8 < p.rank)
-            cp_async_16(dst, p.U + static_cast<size_t>(rp) * p.rank + lane * 8);
-          else
-            st_shared_zero16(dst);
+      // gather this position's U rows into A (the MMAs of position k-1 have
+      // all retired: their last accumulator was consumed).  Two forms, the
+      // same bytes:
+      //  - with several tiles per position (the streaming case), one
+      //    512-byte row per warp instruction (lane j copies 16-byte chunk j
+      //    of the row) by sub-group 0: few, whole-row L2 requests, which
+      //    stay fast while the rings stream;
+      //  - with a single tile per position (ONE_TILE, a small vocabulary: the
+      //    position boundary is all there is), every thread of sub-groups 0 and 1
+      //    loads half of its own row, all loads in flight at once, and
+      //    stores it itself: lower latency when nothing else is in flight.
+      if constexpr (!ONE_TILE) {
+        const int nchunk = sg == 0 ? KB * 8 : 0;
+        for (int r = 0; r < 32 && sg == 0; ++r) {
+          const int rp = __shfl_sync(0xFFFFFFFFu, prev, r);
+          const int rrow = q * 32 + r;
+          const bool rok = (m0 + rrow) < p.N;
+          if (lane < nchunk) {
+            const int kb = lane >> 3, c = lane & 7;
+            const uint32_t dst = a_base + kb * A_KBLOCK_BYTES + rrow * 128 +
+                                 ((c ^ (rrow & 7)) << 4);
+            if (rok && lane * 8 < p.rank)
+              cp_async_16(dst, p.U + static_cast<size_t>(rp) * p.rank + lane * 8);
+            else
+              st_shared_zero16(dst);
+          }
+        }
+        if (sg == 0) {
+          cp_async_commit();
+          cp_async_wait_all();
+        }
+      } else if (sg < 2) {
+        const int kh = sg * 128;  // this thread's half of the row
+        uint4 w[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          w[c] = make_uint4(0u, 0u, 0u, 0u);
+          if (row_ok && kh + c * 8 < p.rank)
+            w[c] = ld_global_nc_v4(p.U + static_cast<size_t>(prev) * p.rank + kh + c * 8);
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int e = kh + c * 8;
+          const int kb = e >> 6, cc = (e & 63) >> 3;
+          st_shared_v4(a_base + kb * A_KBLOCK_BYTES + row * 128 + ((cc ^ (row & 7)) << 4),
+                       w[c]);
         }
       }
-      if (sg == 0) {
-        cp_async_commit();
-        cp_async_wait_all();
+      if (sg == 0 || (ONE_TILE && sg == 1)) {
         fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
         __syncwarp();
         if (lane == 0) mbar_arrive(a_full);
@@ -707,39 +744,31 @@ EncodeTiledFn encode_tiled_fn() {
 }
 
 static std::mutex g_attr_mu;
-static bool g_attr_done[4][128];
+static bool g_attr_done[128];
+
+template <int LDT, bool SAMPLE, int EPI>
+static cudaError_t set_smem_attr() {
+  cudaError_t e = cudaFuncSetAttribute(chain_kernel<LDT, SAMPLE, EPI, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       CHAIN_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(chain_kernel<LDT, SAMPLE, EPI, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              CHAIN_SMEM_BYTES);
+}
 
 static cudaError_t ensure_kernel_attrs(int dev) {
   std::lock_guard<std::mutex> lk(g_attr_mu);
   if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
-  if (!g_attr_done[2][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DSPARK_BF16, true, EPI_SAMPLE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         CHAIN_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(chain_kernel<DSPARK_F32, true, EPI_SAMPLE>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             CHAIN_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    g_attr_done[2][dev] = true;
-  }
-  if (!g_attr_done[0][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DSPARK_BF16, false, EPI_ARGMAX>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         CHAIN_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    g_attr_done[0][dev] = true;
-  }
-  if (!g_attr_done[1][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(chain_kernel<DSPARK_F32, false, EPI_ARGMAX>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         CHAIN_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    g_attr_done[1][dev] = true;
-  }
+  if (g_attr_done[dev]) return cudaSuccess;
+  cudaError_t e;
+  if ((e = set_smem_attr<DSPARK_BF16, true, EPI_SAMPLE>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<DSPARK_F32, true, EPI_SAMPLE>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<DSPARK_BF16, false, EPI_ARGMAX>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<DSPARK_F32, false, EPI_ARGMAX>()) != cudaSuccess) return e;
+  g_attr_done[dev] = true;
   return cudaSuccess;
 }
-
 
 size_t chain_workspace_bytes(int32_t N, int32_t K) {
   const size_t n_mtiles = (static_cast<size_t>(N) + BM - 1) / BM;
@@ -857,18 +886,25 @@ dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // at most one tile per position in every CTA: the widest group is at most
+  // QPT quanta
+  const bool one_tile = (n_quanta + n_vgroups - 1) / n_vgroups <= QPT;
   cudaError_t e;
+#define DSPARK_LAUNCH(LDT, S, E)                                                   \
+  e = one_tile ? cudaLaunchKernelEx(&cfg, chain_kernel<LDT, S, E, true>, tmV, tmL, p) \
+               : cudaLaunchKernelEx(&cfg, chain_kernel<LDT, S, E, false>, tmV, tmL, p)
   if (a.sample) {
     if (a.logits_dtype == DSPARK_BF16)
-      e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_BF16, true, EPI_SAMPLE>, tmV, tmL, p);
+      DSPARK_LAUNCH(DSPARK_BF16, true, EPI_SAMPLE);
     else
-      e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_F32, true, EPI_SAMPLE>, tmV, tmL, p);
+      DSPARK_LAUNCH(DSPARK_F32, true, EPI_SAMPLE);
   } else {
     if (a.logits_dtype == DSPARK_BF16)
-      e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_BF16, false, EPI_ARGMAX>, tmV, tmL, p);
+      DSPARK_LAUNCH(DSPARK_BF16, false, EPI_ARGMAX);
     else
-      e = cudaLaunchKernelEx(&cfg, chain_kernel<DSPARK_F32, false, EPI_ARGMAX>, tmV, tmL, p);
+      DSPARK_LAUNCH(DSPARK_F32, false, EPI_ARGMAX);
   }
+#undef DSPARK_LAUNCH
   if (e == cudaErrorCooperativeLaunchTooLarge) return DSPARK_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return DSPARK_ERR_CUDA;
   return DSPARK_OK;
