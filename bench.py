@@ -471,12 +471,72 @@ def run_gpu(args):
             result["next_stale_select"] = run_stale_select(st, cfg, stream)
             result["next_sample_chain"] = run_sample_chain(st, cfg, stream)
             result["next_lmhead_chain"] = run_lmhead_chain(st, cfg, stream)
+            if cfg.name == "headline":
+                result["workloads"] = run_other_workloads(dev)
         if world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(cfg)
         print(json.dumps(result), flush=True)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def run_other_workloads(dev, names=("tiny", "gemma4_12b", "conc64", "dsv4"),
+                        steps=100):
+    """The same overlapped step (chain on one stream, scheduler alongside on
+    another, verify-token gather after the join; CUDA graphs) on the other
+    workloads of the test plan, timed with CUDA events: per workload the
+    median step, chain and scheduler times and the chain's fractions of the
+    HBM (V-once bytes) and bf16 tensor rooflines.  Stress (8 GB of logits)
+    and DSV4-alt (the DSV4 chain) are left to ``--workload``."""
+    import torch
+    import workloads
+    hbm, tf_burst, _, _ = measured_peaks()
+    out = {}
+    for name in names:
+        cfg = workloads.get_config(name)
+        st = Step(cfg, dev)
+        main, side = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(main):
+            for _ in range(3):
+                st.chain()
+                st.select()
+        main.synchronize()
+        graphs = []
+        for fn, sm in ((st.chain, main), (st.select_nodraft, side), (st.gather, main)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=sm):
+                fn()
+            graphs.append(g)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        for i in range(steps + 5):
+            e = ev[i - 5] if i >= 5 else [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record(main)
+            side.wait_event(e[0])
+            with torch.cuda.stream(main):
+                graphs[0].replay()
+            e[1].record(main)
+            with torch.cuda.stream(side):
+                graphs[1].replay()
+            e[2].record(side)
+            main.wait_event(e[2])
+            with torch.cuda.stream(main):
+                graphs[2].replay()
+            e[3].record(main)
+        torch.cuda.synchronize()
+        assert st.D.dspark_read_status(st.cws) == 0 and st.D.dspark_read_status(st.sws) == 0
+        med = lambda a, b: statistics.median(ev[i][a].elapsed_time(ev[i][b]) * 1e3  # noqa: E731
+                                             for i in range(steps))
+        step_us, chain_us, sel_us = med(0, 3), med(0, 1), med(0, 2)
+        out[name] = {
+            "workload": workload_desc(cfg), "step_us": round(step_us, 2),
+            "chain_us": round(chain_us, 2), "select_us": round(sel_us, 2),
+            "chain_frac_hbm": round(algorithmic_bytes_per_launch(cfg) / (chain_us * 1e-6) / 1e9 / hbm, 4),
+            "chain_frac_tensor": round(flops_per_launch(cfg) / (chain_us * 1e-6) / 1e12 / tf_burst, 4),
+            "steps": steps}
+        del st, graphs
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_greedy_verify(st, cfg, stream, iters=100):
