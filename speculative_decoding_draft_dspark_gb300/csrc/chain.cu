@@ -456,10 +456,9 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
       uint32_t best_key = 0u;  // below every real key
       int best_idx = 0x7FFFFFFF;
       float best_val = -INFINITY;  // the value behind best_key (sampling)
-      // sampling: the row's best published so far by any thread of any CTA
-      // (read one piece ahead), a shared threshold for the skip test
+      // sampling: the row's best published so far by any thread of any CTA,
+      // a shared threshold for the skip test
       uint32_t shared_key = 0u;
-      unsigned long long shared_pend = 0ull;
       unsigned long long *row_slot =
           row_ok ? &p.slots[static_cast<size_t>(k) * p.N + m] : nullptr;
       for (int i = 0; i < nt && ok; ++i, ++ig) {
@@ -541,6 +540,10 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                   }
                 }
                 const int vb = v_tile0 + cb;
+                // the row's shared best, read now and used after the Philox
+                // words (which cover most of the load's latency)
+                const unsigned long long shared_now =
+                    row_slot ? *reinterpret_cast<volatile unsigned long long *>(row_slot) : 0ull;
                 if (vb + SAMPLE_PW > p.vocab) {
 #pragma unroll
                   for (int e = 0; e < SAMPLE_PW; ++e)
@@ -561,9 +564,7 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                 // published key is some element's exact key, so an element
                 // skipped against it (with the margin below) can neither be
                 // the row's winner nor tie with it.
-                shared_key = max(shared_key, static_cast<uint32_t>(shared_pend >> 32));
-                if (row_slot)
-                  shared_pend = *reinterpret_cast<volatile unsigned long long *>(row_slot);
+                shared_key = max(shared_key, static_cast<uint32_t>(shared_now >> 32));
                 if (best_key == 0u && shared_key == 0u) {
                   // nothing to compare with yet: the piece's first element
                   // seeds the threshold with its exact key
