@@ -70,8 +70,10 @@ constexpr int SMEM_USED = SMEM_BAR_OFF + NUM_BARS * 8 + 16;
 constexpr int CHAIN_SMEM_BYTES = SMEM_USED + 1024;  // 1 KB alignment slack
 // warps 0-3 have fixed roles; EPI epilogue warps follow: 8 for the argmax
 // chain (4 / 8 / 12 measured at the headline: chain 311 / 295 / 301 us;
-// Stress 2410 / 2176 / 2157 us), 16 for sampling, whose epilogue does far
-// more arithmetic per element (8 / 12 / 16 / 20: 870 / 822 / 807 / 869 us)
+// Stress 2410 / 2176 / 2157 us), 12 for sampling, whose epilogue does far
+// more arithmetic per element (12 / 16 / 20 / 24 warps with 16-column
+// pieces: 697 / 732 / 737 / 767 us at the headline; more warps leave fewer
+// registers per thread)
 constexpr int chain_threads(int epi) { return (4 + epi) * 32; }
 constexpr int EPI_ARGMAX = 8;
 constexpr int EPI_SAMPLE = 12;
@@ -127,17 +129,52 @@ __device__ __forceinline__ PhiloxKeys philox_keys(uint32_t k0, uint32_t k1) {
   return r;
 }
 
-__device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], const PhiloxKeys &key) {
+// In a position's draws only counter word 0 varies (the vocabulary block);
+// words 1-3 are the request, the position and the offset.  So the product of
+// round 1 that involves word 2, and the product of round 2 that involves the
+// round-1 output word 0, are the same for every draw of a (request,
+// position): computed once per position, they leave 18 of the 20 products
+// per block.  The words are those of the plain rounds, bit for bit.
+struct PhiloxRow {
+  uint32_t c0k;  // offset ^ round-1 key 1 (mixed into round-1 word 2)
+  uint32_t c1k;  // low(M1 * position) ^ round-2 key 0
+  uint32_t c2k;  // high(M0 * a0) ^ round-2 key 1, a0 = round-1 word 0
+  uint32_t d;    // low(M0 * a0): round-2 word 3
+};
+
+__device__ __forceinline__ PhiloxRow philox_row(uint32_t n, uint32_t k, uint32_t offset,
+                                                const PhiloxKeys &key) {
+  const uint64_t p1 = static_cast<uint64_t>(kPhiloxM1) * k;
+  const uint32_t a0 = static_cast<uint32_t>(p1 >> 32) ^ n ^ key.k0[0];
+  const uint64_t q = static_cast<uint64_t>(kPhiloxM0) * a0;
+  PhiloxRow r;
+  r.c0k = offset ^ key.k1[0];
+  r.c1k = static_cast<uint32_t>(p1) ^ key.k0[1];
+  r.c2k = static_cast<uint32_t>(q >> 32) ^ key.k1[1];
+  r.d = static_cast<uint32_t>(q);
+  return r;
+}
+
+// The four words of block (ctr, n, k, offset) given that row's constants.
+__device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t ctr,
+                                              const PhiloxRow &w, const PhiloxKeys &key) {
+  const uint64_t p0 = static_cast<uint64_t>(kPhiloxM0) * ctr;     // round 1
+  const uint32_t n2 = static_cast<uint32_t>(p0 >> 32) ^ w.c0k;
+  const uint64_t p1 = static_cast<uint64_t>(kPhiloxM1) * n2;      // round 2
+  c[0] = static_cast<uint32_t>(p1 >> 32) ^ w.c1k;
+  c[1] = static_cast<uint32_t>(p1);
+  c[2] = static_cast<uint32_t>(p0) ^ w.c2k;
+  c[3] = w.d;
 #pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    const uint64_t p0 = static_cast<uint64_t>(kPhiloxM0) * c[0];
-    const uint64_t p1 = static_cast<uint64_t>(kPhiloxM1) * c[2];
-    const uint32_t n0 = static_cast<uint32_t>(p1 >> 32) ^ c[1] ^ key.k0[r];
-    const uint32_t n2 = static_cast<uint32_t>(p0 >> 32) ^ c[3] ^ key.k1[r];
+  for (int r = 2; r < 10; ++r) {
+    const uint64_t q0 = static_cast<uint64_t>(kPhiloxM0) * c[0];
+    const uint64_t q1 = static_cast<uint64_t>(kPhiloxM1) * c[2];
+    const uint32_t n0 = static_cast<uint32_t>(q1 >> 32) ^ c[1] ^ key.k0[r];
+    const uint32_t m2 = static_cast<uint32_t>(q0 >> 32) ^ c[3] ^ key.k1[r];
     c[0] = n0;
-    c[1] = static_cast<uint32_t>(p1);
-    c[2] = n2;
-    c[3] = static_cast<uint32_t>(p0);
+    c[1] = static_cast<uint32_t>(q1);
+    c[2] = m2;
+    c[3] = static_cast<uint32_t>(q0);
   }
 }
 
@@ -461,6 +498,8 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
       uint32_t shared_key = 0u;
       unsigned long long *row_slot =
           row_ok ? &p.slots[static_cast<size_t>(k) * p.N + m] : nullptr;
+      [[maybe_unused]] const PhiloxRow prow =
+          philox_row(static_cast<uint32_t>(m), static_cast<uint32_t>(k), p.offset, pkeys);
       for (int i = 0; i < nt && ok; ++i, ++ig) {
         const TileGeom g = tile_geom(k, i, qb, qe);
         const int buf = ig & 1;
@@ -480,17 +519,20 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
               smem_u32(smem + SMEM_L_OFF + s * L_STAGE_BYTES) + row * 128;
 #pragma unroll
           for (int c = 0; c < CHUNKS_PER_BOX; ++c) {
-            if (NSG > 1 && (j * CHUNKS_PER_BOX + c) % NSG != sg) continue;
+            // chunks go to the sub-groups by their running index, so that
+            // every warp gets the same share whatever a tile's width
+            if (NSG > 1 && (lit * CHUNKS_PER_BOX + c) % NSG != sg) continue;
             const int col0 = j * LBOX_COLS + c * 32;
             if constexpr (SAMPLE) {
               // Gumbel-max: key = adj / tau + g(n, k, v), g from word v % 4
               // of the Philox block with counter (v / 4, n, k, offset).  An
               // element can beat the running best only if g > best - adj/tau
               // - margin, i.e. 1 - u < 1 - exp(-A) <= A with
-              // A = exp(adj/tau - best + margin).  It is skipped when
-              // u <= 1 - A, with u exact (the mantissa trick below) and
-              // 1 - A rounded down, so that a skip implies 1 - u >= A: the
-              // test costs one ex2 and no logarithm, and the (1 + 2^-10)
+              // A = exp(adj/tau - best + margin).  It is skipped only when
+              // u <= 1 - A provably holds (u exact from the word's mantissa,
+              // the bound on it rounded down), so that a skip implies
+              // 1 - u >= A.  The test costs one ex2 and no logarithm, and
+              // the (1 + 2^-10)
               // factor and the margin cover every rounding and approximation
               // error in A, so a skipped element could never have won.
               // Survivors get the exact key.  The test runs on the FMA pipe
@@ -552,10 +594,8 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                 uint32_t x[SAMPLE_PW];
 #pragma unroll
                 for (int i = 0; i < SAMPLE_PW / 4; ++i) {
-                  uint32_t w4[4] = {static_cast<uint32_t>(vb >> 2) + i,
-                                    static_cast<uint32_t>(m), static_cast<uint32_t>(k),
-                                    p.offset};
-                  philox4x32_10(w4, pkeys);
+                  uint32_t w4[4];
+                  philox4x32_10(w4, static_cast<uint32_t>(vb >> 2) + i, prow, pkeys);
 #pragma unroll
                   for (int j = 0; j < 4; ++j) x[4 * i + j] = w4[j];
                 }
@@ -583,13 +623,13 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
 #pragma unroll
                 for (int e = 0; e < SAMPLE_PW; ++e) {
                   const float A = ex2_approx(fmaf(v[e], s1, s0));
-                  // u = (2 (x >> 9) + 1) 2^-24: 1 + (x >> 9) 2^-23 minus
-                  // 1 - 2^-24, exact by Sterbenz's lemma
-                  const float u = __uint_as_float(mad_hi_u32(x[e], 1u << 23, 0x3F800000u)) -
-                                  0x1.fffffep-1f;
-                  // candidate unless u <= 1 - A (NaN A: always a candidate)
-                  cand_f = fmaf(set_gt_f32(u, __fsub_rd(1.0f, A)), static_cast<float>(1 << e),
-                                cand_f);
+                  // u = u1 - (1 - 2^-24) with u1 = 1 + (x >> 9) 2^-23 (one
+                  // mad.hi).  Skipped when u1 <= RD((2 - 2^-23) - A), which
+                  // implies u <= 1 - 2^-24 - A < 1 - A, so u never needs
+                  // forming (NaN A: always a candidate)
+                  const float u1 = __uint_as_float(mad_hi_u32(x[e], 1u << 23, 0x3F800000u));
+                  cand_f = fmaf(set_gt_f32(u1, __fsub_rd(0x1.fffffep0f, A)),
+                                static_cast<float>(1 << e), cand_f);
                 }
                 uint32_t cand =
                     __float_as_uint(cand_f + 0x1p23f) & ((1u << SAMPLE_PW) - 1u);
