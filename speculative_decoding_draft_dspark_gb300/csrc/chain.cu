@@ -214,7 +214,7 @@ __device__ __forceinline__ float gumbel_from_word(uint32_t x) {
 // ONE_TILE: every CTA owns at most one tile per position (a small
 // vocabulary); the position boundary is then all there is, and A is gathered
 // by two sub-groups each loading half of every row (see the gather below)
-template <int LDT, bool SAMPLE, int EPI, bool ONE_TILE>
+template <int LDT, bool SAMPLE, int EPI, bool ONE_TILE, int REP>
 __global__ void __launch_bounds__(chain_threads(EPI), 1)
     chain_kernel(const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmL,
@@ -402,9 +402,18 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
     const int sg = (warp - 4) >> 2;
     constexpr int NSG = EPI / 4;
     const int row = q * 32 + lane;
-    const int m = m0 + row;
+    // REP > 1 (sampling a batch of at most 64 or 32 requests): the A rows
+    // hold every request REP times and the copies split the vocabulary
+    // chunks, so that the lane quarters that would hold padding rows share
+    // the epilogue's arithmetic.  Copies of a request merge through its
+    // winner slot like the CTAs do.
+    constexpr int RROWS = BM / REP;     // requests per copy
+    const int lrow = REP > 1 ? row % RROWS : row;  // this row's request in the tile
+    const int cp = REP > 1 ? row / RROWS : 0;       // which copy of it
+    const int m = m0 + lrow;
     const bool row_ok = m < p.N;
-    const bool writer = (grp == 0) && row_ok && sg == 0;  // one CTA per tile writes draft
+    // one CTA per tile (and one copy) writes the draft
+    const bool writer = (grp == 0) && row_ok && sg == 0 && cp == 0;
     [[maybe_unused]] const PhiloxKeys pkeys = philox_keys(p.seed_lo, p.seed_hi);
     const uint32_t a_base = smem_u32(smem + SMEM_A_OFF);
     int ig = 0, lit = 0;
@@ -452,7 +461,7 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
         for (int r = 0; r < 32 && sg == 0; ++r) {
           const int rp = __shfl_sync(0xFFFFFFFFu, prev, r);
           const int rrow = q * 32 + r;
-          const bool rok = (m0 + rrow) < p.N;
+          const bool rok = (m0 + (REP > 1 ? rrow % RROWS : rrow)) < p.N;
           if (lane < nchunk) {
             const int kb = lane >> 3, c = lane & 7;
             const uint32_t dst = a_base + kb * A_KBLOCK_BYTES + rrow * 128 +
@@ -516,12 +525,21 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                           wait_bounded(&l_full[s], lph, abort_flag, p.status));
           if (!ok) break;
           const uint32_t box =
-              smem_u32(smem + SMEM_L_OFF + s * L_STAGE_BYTES) + row * 128;
+              smem_u32(smem + SMEM_L_OFF + s * L_STAGE_BYTES) + lrow * 128;
 #pragma unroll
           for (int c = 0; c < CHUNKS_PER_BOX; ++c) {
-            // chunks go to the sub-groups by their running index, so that
-            // every warp gets the same share whatever a tile's width
-            if (NSG > 1 && (lit * CHUNKS_PER_BOX + c) % NSG != sg) continue;
+            // sampling: chunks go to the sub-groups (and copies) by their
+            // running index, so that every warp gets the same share whatever
+            // a tile's width; the argmax chain splits each tile's chunks
+            // (NSG = 2 divides a tile's chunk count)
+            if constexpr (SAMPLE) {
+              if ((NSG > 1 || REP > 1) &&
+                  static_cast<unsigned>(lit * CHUNKS_PER_BOX + c) % (NSG * REP) !=
+                      static_cast<unsigned>(sg * REP + cp))
+                continue;
+            } else {
+              if (NSG > 1 && (j * CHUNKS_PER_BOX + c) % NSG != sg) continue;
+            }
             const int col0 = j * LBOX_COLS + c * 32;
             if constexpr (SAMPLE) {
               // Gumbel-max: key = adj / tau + g(n, k, v), g from word v % 4
@@ -560,7 +578,7 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
 #pragma unroll
                   for (int g8 = 0; g8 < SAMPLE_PW / 8; ++g8) {
                     const int chunk = c * 4 + h * (SAMPLE_PW / 8) + g8;
-                    const uint4 w = ld_shared_v4(box + ((chunk ^ (row & 7)) << 4));
+                    const uint4 w = ld_shared_v4(box + ((chunk ^ (lrow & 7)) << 4));
                     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
@@ -574,7 +592,7 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
 #pragma unroll
                   for (int t = 0; t < SAMPLE_PW / 4; ++t) {
                     const int chunk = (SAMPLE_PW / 4) * h + t;
-                    const uint4 w = ld_shared_v4(box + ((chunk ^ (row & 7)) << 4));
+                    const uint4 w = ld_shared_v4(box + ((chunk ^ (lrow & 7)) << 4));
                     v[4 * t + 0] = __uint_as_float(acc[4 * t + 0]) + __uint_as_float(w.x);
                     v[4 * t + 1] = __uint_as_float(acc[4 * t + 1]) + __uint_as_float(w.y);
                     v[4 * t + 2] = __uint_as_float(acc[4 * t + 2]) + __uint_as_float(w.z);
@@ -606,12 +624,29 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                 // the row's winner nor tie with it.
                 shared_key = max(shared_key, static_cast<uint32_t>(shared_now >> 32));
                 if (best_key == 0u && shared_key == 0u) {
-                  // nothing to compare with yet: the piece's first element
-                  // seeds the threshold with its exact key
-                  const float key0 = fmaf(v[0], p.inv_tau, gumbel_from_word(x[0]));
+                  // nothing to compare with yet: of elements 0, 4, 8 and 12,
+                  // the one with the largest adj seeds the threshold with its
+                  // exact key, published at once (far fewer candidates in the
+                  // first pieces than with a fixed element, for little code)
+                  float vs = v[0];
+                  uint32_t xs = x[0];
+                  int es = 0;
+#pragma unroll
+                  for (int e = 4; e < SAMPLE_PW; e += 4) {
+                    const bool gt = v[e] > vs;
+                    vs = gt ? v[e] : vs;
+                    xs = gt ? x[e] : xs;
+                    es = gt ? e : es;
+                  }
+                  const float key0 = fmaf(vs, p.inv_tau, gumbel_from_word(xs));
                   best_key = f32_key(key0);
-                  best_idx = vb;
+                  best_idx = vb + es;
                   best_val = key0;
+                  if (row_slot)
+                    atomicMax(row_slot,
+                              (static_cast<unsigned long long>(best_key) << 32) |
+                                  static_cast<unsigned long long>(
+                                      0xFFFFFFFFu - static_cast<uint32_t>(best_idx)));
                 }
                 const uint32_t tkey = max(best_key, shared_key);
                 const float tval = tkey == best_key ? best_val : f32_from_key(tkey);
@@ -675,7 +710,7 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                   const int chunk = c * 4 + u;
-                  const uint4 w = ld_shared_v4(box + ((chunk ^ (row & 7)) << 4));
+                  const uint4 w = ld_shared_v4(box + ((chunk ^ (lrow & 7)) << 4));
                   const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                   for (int h = 0; h < 4; ++h) {
@@ -688,7 +723,7 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
               } else {
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                  const uint4 w = ld_shared_v4(box + ((u ^ (row & 7)) << 4));
+                  const uint4 w = ld_shared_v4(box + ((u ^ (lrow & 7)) << 4));
                   v[u * 4 + 0] = __uint_as_float(acc[u * 4 + 0]) + __uint_as_float(w.x);
                   v[u * 4 + 1] = __uint_as_float(acc[u * 4 + 1]) + __uint_as_float(w.y);
                   v[u * 4 + 2] = __uint_as_float(acc[u * 4 + 2]) + __uint_as_float(w.z);
@@ -787,13 +822,13 @@ EncodeTiledFn encode_tiled_fn() {
 static std::mutex g_attr_mu;
 static bool g_attr_done[128];
 
-template <int LDT, bool SAMPLE, int EPI>
+template <int LDT, bool SAMPLE, int EPI, int REP>
 static cudaError_t set_smem_attr() {
-  cudaError_t e = cudaFuncSetAttribute(chain_kernel<LDT, SAMPLE, EPI, false>,
+  cudaError_t e = cudaFuncSetAttribute(chain_kernel<LDT, SAMPLE, EPI, false, REP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        CHAIN_SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(chain_kernel<LDT, SAMPLE, EPI, true>,
+  return cudaFuncSetAttribute(chain_kernel<LDT, SAMPLE, EPI, true, REP>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               CHAIN_SMEM_BYTES);
 }
@@ -803,10 +838,14 @@ static cudaError_t ensure_kernel_attrs(int dev) {
   if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
   if (g_attr_done[dev]) return cudaSuccess;
   cudaError_t e;
-  if ((e = set_smem_attr<DSPARK_BF16, true, EPI_SAMPLE>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<DSPARK_F32, true, EPI_SAMPLE>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<DSPARK_BF16, false, EPI_ARGMAX>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<DSPARK_F32, false, EPI_ARGMAX>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<DSPARK_BF16, true, EPI_SAMPLE, 1>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<DSPARK_BF16, true, EPI_SAMPLE, 2>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<DSPARK_BF16, true, EPI_SAMPLE, 4>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<DSPARK_F32, true, EPI_SAMPLE, 1>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<DSPARK_F32, true, EPI_SAMPLE, 2>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<DSPARK_F32, true, EPI_SAMPLE, 4>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<DSPARK_BF16, false, EPI_ARGMAX, 1>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<DSPARK_F32, false, EPI_ARGMAX, 1>()) != cudaSuccess) return e;
   g_attr_done[dev] = true;
   return cudaSuccess;
 }
@@ -931,20 +970,32 @@ dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream) {
   // QPT quanta
   const bool one_tile = (n_quanta + n_vgroups - 1) / n_vgroups <= QPT;
   cudaError_t e;
-#define DSPARK_LAUNCH(LDT, S, E)                                                   \
-  e = one_tile ? cudaLaunchKernelEx(&cfg, chain_kernel<LDT, S, E, true>, tmV, tmL, p) \
-               : cudaLaunchKernelEx(&cfg, chain_kernel<LDT, S, E, false>, tmV, tmL, p)
+  // sampling a batch of at most 32 (64) requests: every request four
+  // (two) times in the tile's rows
+  const int rep = a.sample ? (a.N <= 32 ? 4 : a.N <= 64 ? 2 : 1) : 1;
+#define DSPARK_LAUNCH(LDT, S, E, R)                                                   \
+  e = one_tile ? cudaLaunchKernelEx(&cfg, chain_kernel<LDT, S, E, true, R>, tmV, tmL, p) \
+               : cudaLaunchKernelEx(&cfg, chain_kernel<LDT, S, E, false, R>, tmV, tmL, p)
+#define DSPARK_LAUNCH_REP(LDT)                 \
+  if (rep == 4)                                \
+    DSPARK_LAUNCH(LDT, true, EPI_SAMPLE, 4);   \
+  else if (rep == 2)                           \
+    DSPARK_LAUNCH(LDT, true, EPI_SAMPLE, 2);   \
+  else                                         \
+    DSPARK_LAUNCH(LDT, true, EPI_SAMPLE, 1)
   if (a.sample) {
-    if (a.logits_dtype == DSPARK_BF16)
-      DSPARK_LAUNCH(DSPARK_BF16, true, EPI_SAMPLE);
-    else
-      DSPARK_LAUNCH(DSPARK_F32, true, EPI_SAMPLE);
+    if (a.logits_dtype == DSPARK_BF16) {
+      DSPARK_LAUNCH_REP(DSPARK_BF16);
+    } else {
+      DSPARK_LAUNCH_REP(DSPARK_F32);
+    }
   } else {
     if (a.logits_dtype == DSPARK_BF16)
-      DSPARK_LAUNCH(DSPARK_BF16, false, EPI_ARGMAX);
+      DSPARK_LAUNCH(DSPARK_BF16, false, EPI_ARGMAX, 1);
     else
-      DSPARK_LAUNCH(DSPARK_F32, false, EPI_ARGMAX);
+      DSPARK_LAUNCH(DSPARK_F32, false, EPI_ARGMAX, 1);
   }
+#undef DSPARK_LAUNCH_REP
 #undef DSPARK_LAUNCH
   if (e == cudaErrorCooperativeLaunchTooLarge) return DSPARK_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return DSPARK_ERR_CUDA;

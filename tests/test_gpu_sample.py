@@ -60,6 +60,9 @@ def test_tiny_workload():
     (257, 3, 4104, 256, "bf16", 1.0),   # three request tiles, ragged both ways
     (64, 9, 5000, 128, "f32", 2.0),
     (200, 4, 65536, 256, "bf16", 1.0),  # many vocabulary tiles per CTA
+    (32, 5, 4104, 128, "bf16", 1.0),    # 32 requests: each held four times
+    (33, 2, 2048, 64, "f32", 1.0),      # 33 requests: each held twice
+    (40, 3, 5000, 64, "bf16", 0.8),     # twice, ragged vocabulary tail
 ])
 def test_shapes(N, K, vocab, rank, dtype, tau):
     from gpu_harness import run_chain, check_chain
@@ -169,7 +172,7 @@ def test_nan_row_and_bad_last_token():
     check_chain(got, score, logits, "f32", U, V, last_ref, sample=SM)
 
 
-@pytest.mark.parametrize("name", ["conc64", "headline"])
+@pytest.mark.parametrize("name", ["gemma4_12b", "conc64", "headline"])
 def test_full_size_workloads(name):
     from gpu_harness import run_chain, check_chain
     cfg = workloads.get_config(name)
