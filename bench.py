@@ -282,6 +282,16 @@ def workload_desc(cfg):
             f"chunked-prefill requests, T={cfg.T}, {cost_desc(cfg)}")
 
 
+def l2_desc(cfg):
+    """How the timed loop relates to the 129 MB L2: the logits stream (and V)
+    of one step against its size."""
+    lb = cfg.N * cfg.K * cfg.vocab * (2 if cfg.logits_dtype == "bf16" else 4)
+    vb = cfg.vocab * cfg.rank * 2
+    big = lb + vb > 129e6
+    return (f"{'inputs larger than' if big else 'inputs within'} L2 (logits "
+            f"{lb / 1e6:.1f} MB, V {vb / 1e6:.1f} MB); no flush")
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -431,7 +441,7 @@ def run_gpu(args):
                        "on one stream" if serial else "scheduler on a second "
                        "stream alongside the chain, verify-token gather after "
                        "the join") + "; CUDA events on the launching streams"),
-            "l2": "inputs larger than L2 (logits 939.5 MB, V 134.2 MB); no flush",
+            "l2": l2_desc(cfg),
             "parallelism": f"replicas x{world}",
         },
         "breakdown_us": {
