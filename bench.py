@@ -330,7 +330,10 @@ def run_gpu(args):
 
     # the three parts of a step: chain (main stream), scheduler (side stream
     # alongside the chain, or main stream after it when --serial) and the
-    # verify-token gather after the join
+    # verify-token gather after the join.  The timed steps replay them as one
+    # CUDA graph per step (no events inside the timed region); a separate
+    # pass replays the parts as three graphs with events between them for
+    # the per-part breakdown.
     if args.no_graph:
         run_chain = st.chain
         run_select = st.select if serial else st.select_nodraft
@@ -348,6 +351,22 @@ def run_gpu(args):
         with torch.cuda.graph(g_gat, stream=stream):
             st.gather()
         run_chain, run_select, run_gather = g_chain.replay, g_sel.replay, g_gat.replay
+        g_step = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step, stream=stream):
+            if serial:
+                st.chain()
+                st.select()
+            else:
+                fork_c = torch.cuda.Event()
+                fork_c.record(stream)
+                side.wait_event(fork_c)
+                st.chain()
+                with torch.cuda.stream(side):
+                    st.select_nodraft()
+                join_c = torch.cuda.Event()
+                join_c.record(side)
+                stream.wait_event(join_c)
+                st.gather()
 
     def step(e=None):
         if serial:
@@ -380,10 +399,16 @@ def run_gpu(args):
         if e is not None:
             e[3].record(stream)
 
+    if args.no_graph:
+        timed_step = step
+    else:
+        def timed_step():
+            with torch.cuda.stream(stream):
+                g_step.replay()
+
     K_steps, W = args.steps, args.warmup
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K_steps)]
     for _ in range(W):
-        step()
+        timed_step()
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
@@ -397,7 +422,7 @@ def run_gpu(args):
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for i in range(K_steps):
-        step(ev[i])
+        timed_step()
     end.record(stream)
     torch.cuda.synchronize()
     t_host = time.perf_counter() - t_host0
@@ -405,12 +430,21 @@ def run_gpu(args):
         dist.barrier()
     clocks = sampler.stop()
     total_ms = start.elapsed_time(end)
-    chain_us = [ev[i][0].elapsed_time(ev[i][1]) * 1e3 for i in range(K_steps)]
+
+    # per-part breakdown (separate pass, events between the parts)
+    n_b = max(1, min(K_steps, 200))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_b)]
+    for _ in range(3):
+        step()
+    for i in range(n_b):
+        step(ev[i])
+    torch.cuda.synchronize()
+    chain_us = [ev[i][0].elapsed_time(ev[i][1]) * 1e3 for i in range(n_b)]
     if serial:
-        sel_us = [ev[i][1].elapsed_time(ev[i][2]) * 1e3 for i in range(K_steps)]
+        sel_us = [ev[i][1].elapsed_time(ev[i][2]) * 1e3 for i in range(n_b)]
     else:  # the scheduler starts with the chain
-        sel_us = [ev[i][0].elapsed_time(ev[i][2]) * 1e3 for i in range(K_steps)]
-    step_us = [ev[i][0].elapsed_time(ev[i][3]) * 1e3 for i in range(K_steps)]
+        sel_us = [ev[i][0].elapsed_time(ev[i][2]) * 1e3 for i in range(n_b)]
+    step_us = [ev[i][0].elapsed_time(ev[i][3]) * 1e3 for i in range(n_b)]
     total_ms = max_over_ranks(total_ms, dev)
 
     # the timed steps raised no device status bit (cheap integrity check)
@@ -437,10 +471,13 @@ def run_gpu(args):
                 "pages' workloads)",
         "config": {
             "workload": workload_desc(cfg),
-            "timing": ("CUDA graphs replayed; " + ("scheduler after the chain "
-                       "on one stream" if serial else "scheduler on a second "
-                       "stream alongside the chain, verify-token gather after "
-                       "the join") + "; CUDA events on the launching streams"),
+            "timing": (("eager launches" if args.no_graph else
+                        "one CUDA graph replayed per step") + "; " +
+                       ("scheduler after the chain on one stream" if serial
+                        else "scheduler on a second stream alongside the "
+                        "chain, verify-token gather after the join") +
+                       "; CUDA events around the timed steps; breakdown_us "
+                       "from a separate pass with events between the parts"),
             "l2": l2_desc(cfg),
             "parallelism": f"replicas x{world}",
         },
@@ -494,10 +531,11 @@ def run_gpu(args):
 def run_other_workloads(dev, names=("tiny", "gemma4_12b", "conc64", "dsv4"),
                         steps=100):
     """The same overlapped step (chain on one stream, scheduler alongside on
-    another, verify-token gather after the join; CUDA graphs) on the other
-    workloads of the test plan, timed with CUDA events: per workload the
-    median step, chain and scheduler times and the chain's fractions of the
-    HBM (V-once bytes) and bf16 tensor rooflines.  Stress (8 GB of logits)
+    another, verify-token gather after the join) on the other workloads of
+    the test plan: the step as one CUDA graph per step with CUDA events
+    around the loop, the chain and scheduler medians from a pass with events
+    between the parts, and the chain's fractions of the HBM (V-once bytes)
+    and bf16 tensor rooflines.  Stress (8 GB of logits)
     and DSV4-alt (the DSV4 chain) are left to ``--workload``."""
     import torch
     import workloads
@@ -534,17 +572,40 @@ def run_other_workloads(dev, names=("tiny", "gemma4_12b", "conc64", "dsv4"),
                 graphs[2].replay()
             e[3].record(main)
         torch.cuda.synchronize()
+        # the step itself: one multi-stream graph per step, events around
+        # all of them
+        g_step = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step, stream=main):
+            f0 = torch.cuda.Event()
+            f0.record(main)
+            side.wait_event(f0)
+            st.chain()
+            with torch.cuda.stream(side):
+                st.select_nodraft()
+            j0 = torch.cuda.Event()
+            j0.record(side)
+            main.wait_event(j0)
+            st.gather()
+        with torch.cuda.stream(main):
+            for _ in range(5):
+                g_step.replay()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(main)
+            for _ in range(steps):
+                g_step.replay()
+            t1.record(main)
+        torch.cuda.synchronize()
         assert st.D.dspark_read_status(st.cws) == 0 and st.D.dspark_read_status(st.sws) == 0
         med = lambda a, b: statistics.median(ev[i][a].elapsed_time(ev[i][b]) * 1e3  # noqa: E731
                                              for i in range(steps))
-        step_us, chain_us, sel_us = med(0, 3), med(0, 1), med(0, 2)
+        step_us, chain_us, sel_us = t0.elapsed_time(t1) * 1e3 / steps, med(0, 1), med(0, 2)
         out[name] = {
             "workload": workload_desc(cfg), "step_us": round(step_us, 2),
             "chain_us": round(chain_us, 2), "select_us": round(sel_us, 2),
             "chain_frac_hbm": round(algorithmic_bytes_per_launch(cfg) / (chain_us * 1e-6) / 1e9 / hbm, 4),
             "chain_frac_tensor": round(flops_per_launch(cfg) / (chain_us * 1e-6) / 1e12 / tf_burst, 4),
             "steps": steps}
-        del st, graphs
+        del st, graphs, g_step
         torch.cuda.empty_cache()
     return out
 
