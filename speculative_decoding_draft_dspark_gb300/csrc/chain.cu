@@ -562,17 +562,12 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
 #pragma unroll 1
               for (int h = 0; h < 32 / SAMPLE_PW; ++h) {
                 const int cb = col0 + h * SAMPLE_PW;
+                static_assert(SAMPLE_PW == 16, "one 16-column tensor-memory load per piece");
                 uint32_t acc[SAMPLE_PW];
-#pragma unroll
-                for (int g8 = 0; g8 < SAMPLE_PW / 8; ++g8) {
-                  uint32_t (&a8)[8] = *reinterpret_cast<uint32_t (*)[8]>(acc + 8 * g8);
-                  tmem_ld_32x32b_x8(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                        static_cast<uint32_t>(buf * BN + cb + 8 * g8),
-                                    a8);
-                }
-#pragma unroll
-                for (int g8 = 0; g8 < SAMPLE_PW / 8; ++g8)
-                  tmem_ld_wait(*reinterpret_cast<uint32_t (*)[8]>(acc + 8 * g8));
+                tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>(buf * BN + cb),
+                                   acc);
+                tmem_ld_wait(acc);
                 float v[SAMPLE_PW];
                 if constexpr (LDT == DSPARK_BF16) {
 #pragma unroll

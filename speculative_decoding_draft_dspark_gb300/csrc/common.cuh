@@ -25,7 +25,9 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity,
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    // sleeps up to 20 us per test (woken by the phase's completion), so
+    // the abort flag and the time limit are still checked that often
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1u;
