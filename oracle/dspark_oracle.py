@@ -13,6 +13,10 @@ What it computes, step by step, with the passage each step follows:
   bias[v] = U[prev] . V[v], and the token is the argmax of the adjusted row.
   prev is the request's last committed token for k = 0, else the token just
   chosen at k - 1.
+* Probabilistic drafting ("Adaptive Verification in vLLM", *Appendix:
+  reproducing*, draft_sample_method "probabilistic"): each token is a draw
+  from softmax(adj / tau), taken as a two-level Gumbel-max over blocks of 16
+  vocabulary entries (sample_position).
 * Survival ("Adaptive Verification in vLLM", *Scheduling the budget*): the
   running product of the confidences along each request.
 * Global top-B (same section): slots of all sampling requests compete on
@@ -113,24 +117,109 @@ def philox4x32_10(c0, c1, c2, c3, k0, k1):
     return c
 
 
-def draft_uniforms(seed: int, offset: int, n: int, k: int, vocab: int) -> np.ndarray:
-    """u[v] in (0, 1) for request n, draft position k, vocabulary entry v.
+# ---------------------------------------------------------------------------
+# probabilistic drafting: a two-level Gumbel-max draw
+# ---------------------------------------------------------------------------
+# Each draft token is a draw from softmax(adj / tau) ("Adaptive Verification
+# in vLLM", *Appendix: reproducing*: draft_sample_method "probabilistic"),
+# taken in two steps over blocks of SAMPLE_BLOCK consecutive vocabulary
+# entries: the block by the Gumbel-max rule on the blocks' log partition
+# functions, then the entry inside the block by inverting its cumulative
+# distribution.  Block j is chosen with probability Z_j / sum Z and entry v of
+# it with probability exp(s_v) / Z_j, so every entry has exactly its softmax
+# probability exp(s_v) / sum Z.
+SAMPLE_BLOCK = 16
 
-    Word v % 4 of Philox4x32-10 with counter (v // 4, n, k, offset) and key
-    (low, high 32 bits of seed), keeping its top 23 bits: u = (2 * (x >> 9) +
-    1) / 2^24, an odd multiple of 2^-24 that fp32 and fp64 both hold exactly.
-    """
-    blocks = np.arange((vocab + 3) // 4, dtype=np.uint64)  # counter word 0
-    words = philox4x32_10(blocks, n, k, offset,
-                          seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)
-    # entry v takes word v % 4 of block v // 4
-    x = np.stack(words, axis=1).reshape(-1)[:vocab]
+
+def word_uniform(x) -> np.ndarray:
+    """u = (2 * (x >> 9) + 1) / 2^24 from a 32-bit word: the top 23 bits, an
+    odd multiple of 2^-24 in (0, 1) that fp32 and fp64 both hold exactly."""
+    x = np.asarray(x, dtype=np.uint64)
     return (2.0 * (x >> np.uint64(9)).astype(np.float64) + 1.0) * 2.0 ** -24
 
 
-def gumbel_noise(seed: int, offset: int, n: int, k: int, vocab: int) -> np.ndarray:
-    """Standard Gumbel noise g = -ln(-ln u) (fp64) from draft_uniforms."""
-    return -np.log(-np.log(draft_uniforms(seed, offset, n, k, vocab)))
+def block_words(seed: int, offset: int, n: int, k: int, n_blocks: int):
+    """The two words of every block j of request n, draft position k:
+    Philox4x32-10 with counter (j // 2, n, k, offset) and key (low, high 32
+    bits of seed); an even block takes words 0 and 1, an odd one words 2 and
+    3.  Returns (x_gumbel, x_choice), uint64 arrays of n_blocks."""
+    ctr = np.arange((n_blocks + 1) // 2, dtype=np.uint64)
+    w = philox4x32_10(ctr, n, k, offset, seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)
+    xg = np.stack([w[0], w[2]], axis=1).reshape(-1)[:n_blocks]
+    xc = np.stack([w[1], w[3]], axis=1).reshape(-1)[:n_blocks]
+    return xg, xc
+
+
+def _block_view(s: np.ndarray) -> np.ndarray:
+    """s [rows, vocab] as [rows, n_blocks, SAMPLE_BLOCK], -inf past vocab."""
+    rows, vocab = s.shape
+    nb = -(-vocab // SAMPLE_BLOCK)
+    pad = np.full((rows, nb * SAMPLE_BLOCK), -np.inf)
+    pad[:, :vocab] = s
+    return pad.reshape(rows, nb, SAMPLE_BLOCK)
+
+
+def _block_log_partition(b: np.ndarray) -> np.ndarray:
+    """log sum exp over the last axis: NaN if any entry is NaN, -inf if every
+    entry is -inf (max-shifted, fp64)."""
+    m = np.max(b, axis=-1)                    # NaN propagates
+    finite = np.isfinite(m)
+    mm = np.where(finite, m, 0.0)
+    with np.errstate(invalid="ignore"):
+        z = np.sum(np.exp(b - mm[..., None]), axis=-1)
+    return np.where(finite, mm + np.log(np.where(finite, z, 1.0)), m)
+
+
+def _within_block(b: np.ndarray, u: float) -> int:
+    """The entry of one block drawn with u in (0, 1): the first NaN entry if
+    there is one, the first entry if all are -inf, else the first e with
+    sum_{i <= e} exp(b_i - max) > u * sum_i exp(b_i - max)."""
+    if np.isnan(b).any():
+        return int(np.argmax(np.isnan(b)))
+    m = np.max(b)
+    if m == -np.inf:
+        return 0
+    c = np.cumsum(np.exp(b - m))
+    return int(np.argmax(c > u * c[-1]))
+
+
+def sample_position(adj: np.ndarray, tau: float, seed: int, offset: int,
+                    ns, k: int) -> dict:
+    """Draws one token per row of adj [rows, vocab] (fp64) from
+    softmax(adj / tau); row i uses the random words of request ns[i] and
+    draft position k.  Returns the tokens, the score (the winning block's key
+    log Z_j + g_j), the top-2 margin and |max| of the block keys, and per row
+    the block keys, the winning block's cumulative weights and the choice
+    target u * total (for the parity tests' tolerance)."""
+    s = np.asarray(adj, dtype=np.float64) / tau
+    b = _block_view(s)
+    rows, nb, _ = b.shape
+    keys = np.empty((rows, nb))
+    uc = np.empty((rows, nb))
+    for i, n in enumerate(ns):
+        xg, xc = block_words(seed, offset, int(n), k, nb)
+        keys[i] = _block_log_partition(b[i]) - np.log(-np.log(word_uniform(xg)))
+        uc[i] = word_uniform(xc)
+    jstar = np.argmax(keys, axis=1)           # first NaN, else first maximum
+    r = np.arange(rows)
+    best = keys[r, jstar]
+    tok = np.array([jstar[i] * SAMPLE_BLOCK + _within_block(b[i, jstar[i]], uc[i, jstar[i]])
+                    for i in range(rows)], dtype=np.int64)
+    if nb > 1:
+        part = np.partition(keys, nb - 2, axis=1)[:, -2:]
+        with np.errstate(invalid="ignore"):
+            margin = np.where(np.isnan(best), np.nan, part[:, 1] - part[:, 0])
+    else:
+        margin = np.full(rows, np.inf)
+    cum, target = [], []
+    for i in range(rows):
+        bb = b[i, jstar[i]]
+        m = np.max(bb)
+        c = np.cumsum(np.exp(bb - m)) if np.isfinite(m) else np.zeros(SAMPLE_BLOCK)
+        cum.append(c)
+        target.append(uc[i, jstar[i]] * c[-1])
+    return dict(tok=tok, score=best, margin=margin, absmax=np.abs(best), keys=keys,
+                block=jstar, cum=np.array(cum), target=np.array(target))
 
 
 # ---------------------------------------------------------------------------
@@ -142,19 +231,13 @@ def markov_bias(U64: np.ndarray, V64: np.ndarray, prev: np.ndarray) -> np.ndarra
 
 
 def chain_position(logits_k64: np.ndarray, U64: np.ndarray, V64: np.ndarray,
-                   prev: np.ndarray, noise: np.ndarray | None = None,
-                   tau: float = 1.0) -> dict:
+                   prev: np.ndarray) -> dict:
     """One draft position: adjusted logits and their first-index argmax.
 
     numpy's argmax returns the first maximal index and the first NaN if a row
-    holds one, which is the tie and NaN rule of the C ABI.  With ``noise``
-    (Gumbel values per row and token) the token is drawn from the softmax of
-    adj / tau by the Gumbel-max rule: the argmax of adj / tau + noise; the
-    score is then that perturbed value.
+    holds one, which is the tie and NaN rule of the C ABI.
     """
     adj = logits_k64 + markov_bias(U64, V64, prev)
-    if noise is not None:
-        adj = adj / tau + noise
     tok = np.argmax(adj, axis=1)
     rows = np.arange(adj.shape[0])
     best = adj[rows, tok]
@@ -183,10 +266,9 @@ def chain(logits: np.ndarray, logits_dtype: str, U: np.ndarray, V: np.ndarray,
     ``sample`` = dict(seed, offset, tau) draws every token from the softmax
     of the adjusted logits at temperature tau instead of taking the argmax
     (probabilistic drafting: "Adaptive Verification in vLLM", *Appendix:
-    reproducing*, draft_sample_method "probabilistic"), by the Gumbel-max
-    rule with gumbel_noise; ``rows`` gives each row's request index n for the
-    noise counters (default 0..n-1).  Scores, margins and |max| then refer to
-    adj / tau + noise.
+    reproducing*, draft_sample_method "probabilistic"), by sample_position;
+    ``rows`` gives each row's request index n for the random words (default
+    0..n-1).  Scores, margins and |max| then refer to the block keys.
     """
     U64 = bf16_to_f64(U)
     V64 = bf16_to_f64(V)
@@ -204,12 +286,12 @@ def chain(logits: np.ndarray, logits_dtype: str, U: np.ndarray, V: np.ndarray,
     adjs = []
     rows = np.arange(n) if rows is None else np.asarray(rows)
     for k in range(K):
-        noise = None
+        r = chain_position(to_f64(logits[:, k, :], logits_dtype), U64, V64, prev)
         if sample is not None:
-            noise = np.stack([gumbel_noise(int(sample["seed"]), int(sample["offset"]),
-                                           int(rr), k, vocab) for rr in rows])
-        r = chain_position(to_f64(logits[:, k, :], logits_dtype), U64, V64, prev,
-                           noise, float(sample["tau"]) if sample is not None else 1.0)
+            adj = r["adj"]
+            r = sample_position(adj, float(sample["tau"]), int(sample["seed"]),
+                                int(sample["offset"]), rows, k)
+            r["adj"] = adj
         draft[:, k] = r["tok"]
         score[:, k] = r["score"]
         margin[:, k] = r["margin"]

@@ -1,13 +1,16 @@
-"""Pins of the oracle's probabilistic drafting (Gumbel-max over the adjusted
-logits with Philox4x32-10 noise).
+"""Pins of the oracle's probabilistic drafting: a two-level Gumbel-max draw
+over blocks of 16 vocabulary entries with Philox4x32-10 words.
 
 "Adaptive Verification in vLLM", *Appendix: reproducing*: the drafter runs
 with draft_sample_method "probabilistic", i.e. each draft token is drawn
 from the adjusted distribution instead of taken as its argmax.  The random
-numbers come from Philox4x32-10 (Salmon et al., SC 2011), pinned here by its
-published known-answer vectors; the sampling rule is pinned by its
-distribution (chi-square against the softmax), its zero-temperature limit
-(the greedy oracle) and a chain whose bias forces the next token.
+words come from Philox4x32-10 (Salmon et al., SC 2011), pinned here by its
+published known-answer vectors.  The sampling rule is pinned by its
+distribution (chi-square against the softmax over several blocks, a
+ragged last block included), with planted mistakes in each of its steps
+failing that pin; by closed forms (one block of equal entries, blocks with
+one finite entry, NaN and -inf rows); by its zero-temperature limit (the
+greedy oracle) and by a chain whose bias forces the next token.
 """
 import json
 import math
@@ -17,8 +20,10 @@ import numpy as np
 import pytest
 
 import oracle
+from oracle import dspark_oracle as O
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
+G = O.SAMPLE_BLOCK
 
 
 def test_philox_known_answers():
@@ -32,55 +37,125 @@ def test_philox_known_answers():
 
 
 def test_uniforms_exact_and_in_range():
-    u = oracle.draft_uniforms(seed=0x1234_5678_9ABC, offset=3, n=5, k=2, vocab=4096)
-    assert np.all((u > 0) & (u < 1))
-    assert np.array_equal(u.astype(np.float32).astype(np.float64), u)
-    m = u * 2.0 ** 24
-    assert np.array_equal(m, np.round(m)) and np.all(np.round(m) % 2 == 1)
-    # word v % 4 of counter v // 4: recompute four entries by hand
+    xg, xc = oracle.block_words(seed=0x1234_5678_9ABC, offset=3, n=5, k=2, n_blocks=4096)
+    for x in (xg, xc):
+        u = oracle.word_uniform(x)
+        assert np.all((u > 0) & (u < 1))
+        assert np.array_equal(u.astype(np.float32).astype(np.float64), u)
+        m = u * 2.0 ** 24
+        assert np.array_equal(m, np.round(m)) and np.all(np.round(m) % 2 == 1)
+    # blocks 2 and 3 take the words of counter 1: 0, 1 and 2, 3
     seed = 0x1234_5678_9ABC
     w = oracle.philox4x32_10(1, 5, 2, 3, seed & 0xFFFFFFFF, seed >> 32)
-    for j in range(4):
-        assert u[4 + j] == (2 * (int(w[j]) >> 9) + 1) * 2.0 ** -24
+    assert (int(xg[2]), int(xc[2]), int(xg[3]), int(xc[3])) == tuple(int(x) for x in w)
 
 
 def test_streams_differ_by_every_counter_field():
-    base = oracle.draft_uniforms(7, 0, 0, 0, 64)
+    base = oracle.block_words(7, 0, 0, 0, 64)[0]
     for kw in (dict(seed=8, offset=0, n=0, k=0), dict(seed=7, offset=1, n=0, k=0),
                dict(seed=7, offset=0, n=1, k=0), dict(seed=7, offset=0, n=0, k=1),
                dict(seed=7 + (1 << 32), offset=0, n=0, k=0)):
-        other = oracle.draft_uniforms(vocab=64, **kw)
+        other = oracle.block_words(n_blocks=64, **kw)[0]
         assert np.mean(other == base) < 0.05
 
 
 def test_gumbel_moments():
-    """Standard Gumbel: mean = Euler-Mascheroni constant, variance = pi^2/6."""
-    g = np.concatenate([oracle.gumbel_noise(11, off, 0, 0, 1 << 16) for off in range(8)])
+    """Standard Gumbel from the block words: mean = Euler-Mascheroni
+    constant, variance = pi^2/6."""
+    x = np.concatenate([oracle.block_words(11, off, 0, 0, 1 << 15)[0] for off in range(8)])
+    g = -np.log(-np.log(oracle.word_uniform(x)))
     n = g.size
-    mean, var = g.mean(), g.var()
-    assert abs(mean - 0.5772156649015329) < 5 * math.sqrt(math.pi ** 2 / 6 / n)
+    assert abs(g.mean() - 0.5772156649015329) < 5 * math.sqrt(math.pi ** 2 / 6 / n)
     # the variance of the sample variance of a Gumbel: (mu4 - sigma^4) / n,
     # mu4 = 27/5 sigma^4 (excess kurtosis 12/5)
     s2 = math.pi ** 2 / 6
-    assert abs(var - s2) < 5 * math.sqrt((27 / 5 - 1) * s2 ** 2 / n)
+    assert abs(g.var() - s2) < 5 * math.sqrt((27 / 5 - 1) * s2 ** 2 / n)
 
 
-@pytest.mark.parametrize("tau", [1.0, 0.5, 2.0])
-def test_sampling_matches_softmax(tau):
-    """Tokens drawn with the chain's rule follow softmax(adj / tau)."""
-    adj = np.array([[1.0, 0.0, 2.5, -1.0, 2.0, 0.5]])
-    V = adj.shape[1]
-    S = 20000
-    counts = np.zeros(V)
-    U64 = np.zeros((V, 1))
-    for off in range(S):
-        noise = oracle.gumbel_noise(99, off, 0, 0, V)[None, :]
-        r = oracle.chain_position(adj, U64, U64, np.zeros(1, np.int64), noise, tau)
-        counts[r["tok"][0]] += 1
-    p = np.exp(adj[0] / tau - np.max(adj[0] / tau))
+# three blocks (16, 16 and a ragged 5) of very different masses and shapes
+ADJ = np.concatenate([np.linspace(-1.0, 2.0, 16), np.full(16, 0.5),
+                      np.array([3.0, -2.0, 1.0, 0.0, 2.5])])
+S_DRAWS = 30000
+
+
+def _chi2(tau):
+    s = oracle.sample_position(np.tile(ADJ, (S_DRAWS, 1)), tau, seed=99, offset=4,
+                               ns=np.arange(S_DRAWS), k=1)
+    counts = np.bincount(s["tok"], minlength=ADJ.size)
+    p = np.exp(ADJ / tau - np.max(ADJ / tau))
     p /= p.sum()
-    chi2 = float(np.sum((counts - S * p) ** 2 / (S * p)))
-    assert chi2 < 30.0, (chi2, counts, S * p)      # df = 5: p-value ~ 1.5e-5
+    return float(np.sum((counts - S_DRAWS * p) ** 2 / (S_DRAWS * p)))
+
+
+# df = 36; P(chi2 > 80) is about 3e-5
+CHI2_LIMIT = 80.0
+
+
+@pytest.mark.parametrize("tau", [1.0, 0.7])
+def test_sampling_matches_softmax(tau):
+    """Tokens drawn by the two-level rule follow softmax(adj / tau)."""
+    chi2 = _chi2(tau)
+    assert chi2 < CHI2_LIMIT, chi2
+
+
+def test_planted_mistakes_fail_the_distribution(monkeypatch):
+    """Each step of the rule, done wrong, moves the draws off the softmax."""
+    # block weight: its largest entry instead of its log partition function
+    with monkeypatch.context() as m:
+        m.setattr(O, "_block_log_partition", lambda b: np.max(b, axis=-1))
+        assert _chi2(1.0) > CHI2_LIMIT
+    # entry inside the block: uniform instead of by weight
+    with monkeypatch.context() as m:
+        m.setattr(O, "_within_block",
+                  lambda b, u: int(min(int(u * np.sum(np.isfinite(b))), G - 1)))
+        assert _chi2(1.0) > CHI2_LIMIT
+    # the entry drawn with the block's Gumbel word instead of its own word
+    real = O.block_words
+    with monkeypatch.context() as m:
+        m.setattr(O, "block_words", lambda *a: (real(*a)[0], real(*a)[0]))
+        assert _chi2(1.0) > CHI2_LIMIT
+
+
+def test_one_block_of_equal_entries_is_the_floor():
+    """Equal weights: the inverse CDF picks floor(16 u) (16 u is never an
+    integer for u an odd multiple of 2^-24)."""
+    xg, xc = oracle.block_words(3, 8, 2, 5, 1)
+    u = float(oracle.word_uniform(xc)[0])
+    r = oracle.sample_position(np.full((1, G), 0.25), 1.0, 3, 8, [2], 5)
+    assert r["tok"][0] == math.floor(G * u)
+    # and the score is log(16 * e^0.25) + g
+    g = -math.log(-math.log(float(oracle.word_uniform(xg)[0])))
+    assert abs(r["score"][0] - (0.25 + math.log(16.0) + g)) < 1e-12
+
+
+def test_blocks_with_one_finite_entry_reduce_to_gumbel_max():
+    """With one finite entry per block the block key is that entry plus its
+    block's Gumbel, and the draw is that entry: plain Gumbel-max over them."""
+    nb = 6
+    adj = np.full((1, nb * G), -np.inf)
+    vals = np.array([0.5, 1.25, -3.0, 2.0, 0.0, 1.0])
+    pos = np.array([3, 0, 15, 7, 9, 1])
+    adj[0, np.arange(nb) * G + pos] = vals
+    xg, _ = oracle.block_words(21, 2, 4, 3, nb)
+    key = vals - np.log(-np.log(oracle.word_uniform(xg)))
+    r = oracle.sample_position(adj, 1.0, 21, 2, [4], 3)
+    j = int(np.argmax(key))
+    assert r["tok"][0] == j * G + pos[j]
+    assert r["score"][0] == key[j]
+    top2 = np.sort(key)[-2:]
+    assert r["margin"][0] == top2[1] - top2[0]
+
+
+def test_nan_and_minus_infinity_rows():
+    adj = np.random.default_rng(1).standard_normal((3, 50))
+    adj[0, 20] = np.nan
+    adj[0, 3] = np.nan           # the first NaN wins, whatever the noise
+    adj[1, :] = -np.inf          # nothing finite: the first entry
+    adj[2, 40:] = -np.inf        # a ragged, partly -inf last block
+    r = oracle.sample_position(adj, 1.0, 5, 0, [0, 1, 2], 0)
+    assert r["tok"][0] == 3 and np.isnan(r["score"][0])
+    assert r["tok"][1] == 0 and r["score"][1] == -np.inf
+    assert r["tok"][2] < 40
 
 
 def _factors(vocab, rank):
