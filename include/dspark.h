@@ -127,19 +127,24 @@ DSPARK_API dspark_status dspark_chain_draft(
  * reproducing": the drafter runs with draft_sample_method "probabilistic",
  * drawing each draft token from the adjusted distribution instead of taking
  * its argmax.  Same chain, same arguments and limits as dspark_chain_draft,
- * except that draft[n,k] is the first index of the maximum of
- *     adj[n,k,v] / temperature + g(n, k, v),
- * the Gumbel-max rule, so draft[n,k] ~ softmax(adj[n,k,:] / temperature)
- * given the earlier tokens.  The noise g = -ln(-ln u) comes from a
- * counter-based generator: x = word (v % 4) of Philox4x32-10 (Salmon et al.,
- * SC 2011) with counter (v / 4, n, k, offset) and key (seed low 32 bits,
- * seed high 32 bits), u = (2 (x >> 9) + 1) / 2^24; noise is fp32 (accurate
- * logf).  The same (seed, offset) reproduces the same drafts; a caller
- * advances offset every decoding step.
+ * except that draft[n,k] ~ softmax(adj[n,k,:] / temperature) given the
+ * earlier tokens, drawn in two steps over blocks of 16 vocabulary entries
+ * (block j = entries 16j .. 16j+15): the block with the largest
+ *     key_j = log sum_{v in j} exp(adj[n,k,v] / temperature) + g_j,
+ * g_j = -ln(-ln u_j) (the Gumbel-max rule over blocks: block j wins with
+ * probability Z_j / sum Z), then the first entry of that block whose
+ * cumulative weight exp(adj / temperature) exceeds c_j times the block's
+ * total (entry v wins with probability exp(adj_v / temperature) / Z_j).  A
+ * block holding a NaN has key NaN, NaN ranks highest, and its entry is its
+ * first NaN; ties go to the lower index.  u_j and c_j come from a
+ * counter-based generator: words 2 (j % 2) and 2 (j % 2) + 1 of
+ * Philox4x32-10 (Salmon et al., SC 2011) with counter (j / 2, n, k, offset)
+ * and key (seed low 32 bits, seed high 32 bits), u = (2 (x >> 9) + 1) / 2^24
+ * for a word x; the keys are fp32.  The same (seed, offset) reproduces the
+ * same drafts; a caller advances offset every decoding step.
  * temperature  > 0 and finite with a finite reciprocal, else
  *              DSPARK_ERR_INVALID_ARG.
- * draft_score  optional out [N, K]: the perturbed value adj/temperature + g
- *              at draft[n,k].
+ * draft_score  optional out [N, K]: the winning block's key key_j.
  * ------------------------------------------------------------------------ */
 DSPARK_API dspark_status dspark_chain_sample(
     const void *logits, int32_t logits_dtype,

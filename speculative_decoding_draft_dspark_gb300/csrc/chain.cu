@@ -27,9 +27,10 @@
 //
 // Probabilistic drafting ("Adaptive Verification in vLLM", section "Appendix:
 // reproducing", draft_sample_method "probabilistic") is the same kernel with
-// SAMPLE set: the epilogue adds Gumbel noise from Philox4x32-10 to adj / tau
-// before the maximum (the Gumbel-max rule), so each token is a draw from the
-// softmax of the adjusted logits.
+// SAMPLE set: each token is a draw from the softmax of adj / tau, taken as a
+// Gumbel-max over blocks of 16 vocabulary entries (keyed on each block's log
+// partition function, noise from Philox4x32-10) and then the entry inside
+// the winning block; the running (key, index) maximum is combined as above.
 //
 // Warp roles (one CTA per SM, all 512 TMEM columns):
 //   warp 0      TMA producer of V tiles (4 K-blocks of 64 per tile)
@@ -77,7 +78,7 @@ constexpr int CHAIN_SMEM_BYTES = SMEM_USED + 1024;  // 1 KB alignment slack
 constexpr int chain_threads(int epi) { return (4 + epi) * 32; }
 constexpr int EPI_ARGMAX = 8;
 constexpr int EPI_SAMPLE = 12;
-constexpr int SAMPLE_PW = 16;  // columns per step of the sampling epilogue
+constexpr int SAMPLE_BLOCK = 16;  // vocabulary entries per block of the sampling draw
 constexpr uint32_t TMEM_COLS = 512;  // two 256-column fp32 accumulators
 // bytes of V worth protecting in L2 across positions (measured on GB300:
 // with a 128 MiB V, protecting 6 tenths is fastest for batches of 8 to 256
@@ -542,37 +543,41 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
             }
             const int col0 = j * LBOX_COLS + c * 32;
             if constexpr (SAMPLE) {
-              // Gumbel-max: key = adj / tau + g(n, k, v), g from word v % 4
-              // of the Philox block with counter (v / 4, n, k, offset).  An
-              // element can beat the running best only if g > best - adj/tau
-              // - margin, i.e. 1 - u < 1 - exp(-A) <= A with
-              // A = exp(adj/tau - best + margin).  It is skipped only when
-              // u <= 1 - A provably holds (u exact from the word's mantissa,
-              // the bound on it rounded down), so that a skip implies
-              // 1 - u >= A.  The test costs one ex2 and no logarithm, and
-              // the (1 + 2^-10)
-              // factor and the margin cover every rounding and approximation
-              // error in A, so a skipped element could never have won.
-              // Survivors get the exact key.  The test runs on the FMA pipe
-              // (mad.hi for the mantissa, the candidate mask accumulated in
-              // fp32), leaving the integer pipe to Philox.  The chunk is
-              // taken SAMPLE_PW columns at a time in a rolled loop: the fully
-              // unrolled form does not fit the instruction cache.
+              // Two-level Gumbel-max draw over blocks of 16 vocabulary
+              // entries (a piece is one block, j = v / 16): the block by the
+              // Gumbel-max rule on key_j = L_j + g_j, L_j = log sum exp(adj /
+              // tau) over the block, then the entry inside the winning block
+              // by inverting its cumulative weights with a second uniform.
+              // Block j takes words 2 (j % 2) and 2 (j % 2) + 1 of the Philox
+              // block with counter (j / 2, n, k, offset): one Philox block
+              // per 32-column chunk.  Since L_j <= max_j / tau + ln 16, a
+              // block can beat the running best only if g_j > best - margin
+              // - max_j / tau - ln 16, i.e. 1 - u < 1 - exp(-A) <= A with
+              // A = exp(max_j / tau + ln 16 - best + margin).  It is skipped
+              // only when u <= 1 - A provably holds (u exact from the word's
+              // mantissa, the bound on it rounded down): one ex2 and no
+              // logarithm per block, the (1 + 2^-10) factor and the margin
+              // covering every rounding and approximation error in A.  Blocks
+              // that pass get their exact key, and their entry when the key
+              // beats the running best.
+              static_assert(SAMPLE_BLOCK == 16, "one 16-column tensor-memory load per block");
               const float s1 = p.inv_tau * 1.4426950408889634f;
+              const int vc = v_tile0 + col0;  // a multiple of 32
+              uint32_t wd[4];
+              philox4x32_10(wd, static_cast<uint32_t>(vc >> 5), prow, pkeys);
 #pragma unroll 1
-              for (int h = 0; h < 32 / SAMPLE_PW; ++h) {
-                const int cb = col0 + h * SAMPLE_PW;
-                static_assert(SAMPLE_PW == 16, "one 16-column tensor-memory load per piece");
-                uint32_t acc[SAMPLE_PW];
+              for (int h = 0; h < 2; ++h) {
+                const int cb = col0 + h * SAMPLE_BLOCK;
+                uint32_t acc[SAMPLE_BLOCK];
                 tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        static_cast<uint32_t>(buf * BN + cb),
                                    acc);
                 tmem_ld_wait(acc);
-                float v[SAMPLE_PW];
+                float v[SAMPLE_BLOCK];
                 if constexpr (LDT == DSPARK_BF16) {
 #pragma unroll
-                  for (int g8 = 0; g8 < SAMPLE_PW / 8; ++g8) {
-                    const int chunk = c * 4 + h * (SAMPLE_PW / 8) + g8;
+                  for (int g8 = 0; g8 < 2; ++g8) {
+                    const int chunk = c * 4 + h * 2 + g8;
                     const uint4 w = ld_shared_v4(box + ((chunk ^ (lrow & 7)) << 4));
                     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -585,8 +590,8 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                   }
                 } else {
 #pragma unroll
-                  for (int t = 0; t < SAMPLE_PW / 4; ++t) {
-                    const int chunk = (SAMPLE_PW / 4) * h + t;
+                  for (int t = 0; t < 4; ++t) {
+                    const int chunk = 4 * h + t;
                     const uint4 w = ld_shared_v4(box + ((chunk ^ (lrow & 7)) << 4));
                     v[4 * t + 0] = __uint_as_float(acc[4 * t + 0]) + __uint_as_float(w.x);
                     v[4 * t + 1] = __uint_as_float(acc[4 * t + 1]) + __uint_as_float(w.y);
@@ -595,103 +600,87 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                   }
                 }
                 const int vb = v_tile0 + cb;
-                // the row's shared best, read now and used after the Philox
-                // words (which cover most of the load's latency)
+                // the row's shared best (its latency overlaps the block max)
                 const unsigned long long shared_now =
                     row_slot ? *reinterpret_cast<volatile unsigned long long *>(row_slot) : 0ull;
-                if (vb + SAMPLE_PW > p.vocab) {
+                if (vb + SAMPLE_BLOCK > p.vocab) {
 #pragma unroll
-                  for (int e = 0; e < SAMPLE_PW; ++e)
+                  for (int e = 0; e < SAMPLE_BLOCK; ++e)
                     if (vb + e >= p.vocab) v[e] = -INFINITY;
                 }
-                uint32_t x[SAMPLE_PW];
+                float mx = v[0];  // NaN if the block holds one
 #pragma unroll
-                for (int i = 0; i < SAMPLE_PW / 4; ++i) {
-                  uint32_t w4[4];
-                  philox4x32_10(w4, static_cast<uint32_t>(vb >> 2) + i, prow, pkeys);
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) x[4 * i + j] = w4[j];
-                }
+                for (int e = 1; e < SAMPLE_BLOCK; ++e) mx = fmax_nan(mx, v[e]);
+                const uint32_t xg = h ? wd[2] : wd[0];  // the block's Gumbel word
+                const uint32_t xc = h ? wd[3] : wd[1];  // the word of its entry
                 // The skip test's threshold: this thread's best or the row's
                 // best published by any thread, whichever is larger.  Every
-                // published key is some element's exact key, so an element
-                // skipped against it (with the margin below) can neither be
-                // the row's winner nor tie with it.
+                // published key is some block's exact key, so a block skipped
+                // against it (with the margin below) can neither win nor tie.
                 shared_key = max(shared_key, static_cast<uint32_t>(shared_now >> 32));
-                if (best_key == 0u && shared_key == 0u) {
-                  // nothing to compare with yet: of elements 0, 4, 8 and 12,
-                  // the one with the largest adj seeds the threshold with its
-                  // exact key, published at once (far fewer candidates in the
-                  // first pieces than with a fixed element, for little code)
-                  float vs = v[0];
-                  uint32_t xs = x[0];
-                  int es = 0;
-#pragma unroll
-                  for (int e = 4; e < SAMPLE_PW; e += 4) {
-                    const bool gt = v[e] > vs;
-                    vs = gt ? v[e] : vs;
-                    xs = gt ? x[e] : xs;
-                    es = gt ? e : es;
-                  }
-                  const float key0 = fmaf(vs, p.inv_tau, gumbel_from_word(xs));
-                  best_key = f32_key(key0);
-                  best_idx = vb + es;
-                  best_val = key0;
-                  if (row_slot)
-                    atomicMax(row_slot,
-                              (static_cast<unsigned long long>(best_key) << 32) |
-                                  static_cast<unsigned long long>(
-                                      0xFFFFFFFFu - static_cast<uint32_t>(best_idx)));
-                }
                 const uint32_t tkey = max(best_key, shared_key);
                 const float tval = tkey == best_key ? best_val : f32_from_key(tkey);
-                const bool none = tval != tval;
+                const bool none = tkey == 0u || tval != tval;  // nothing to beat yet
                 const float margin = 1e-4f * (1.0f + fabsf(tval));
                 const float s0 = none ? INFINITY
-                                      : (margin - tval) * 1.4426950408889634f + 0x1p-10f;
-                float cand_f = 0.0f;  // sum of 2^e over the candidates
+                                      : (margin - tval) * 1.4426950408889634f + 0x1p-10f + 4.0f;
+                const float A = ex2_approx(fmaf(mx, s1, s0));
+                // u = u1 - (1 - 2^-24) with u1 = 1 + (xg >> 9) 2^-23 (one
+                // mad.hi); u1 <= RD((2 - 2^-23) - A) implies u < 1 - A (NaN A:
+                // always a candidate)
+                const float u1 = __uint_as_float(mad_hi_u32(xg, 1u << 23, 0x3F800000u));
+                const bool cand = !(u1 <= __fsub_rd(0x1.fffffep0f, A));
+                if (__any_sync(0xFFFFFFFFu, cand) && cand) {
+                  // the block's exact key: NaN if it holds a NaN (the first
+                  // NaN is then its entry), -inf if nothing in it is finite
+                  float key, sum = 0.0f;
+                  float ex[SAMPLE_BLOCK];
+                  int e_star = 0;
+                  const bool finite = mx == mx && mx != -INFINITY;
+                  if (mx != mx) {
+                    key = mx;
 #pragma unroll
-                for (int e = 0; e < SAMPLE_PW; ++e) {
-                  const float A = ex2_approx(fmaf(v[e], s1, s0));
-                  // u = u1 - (1 - 2^-24) with u1 = 1 + (x >> 9) 2^-23 (one
-                  // mad.hi).  Skipped when u1 <= RD((2 - 2^-23) - A), which
-                  // implies u <= 1 - 2^-24 - A < 1 - A, so u never needs
-                  // forming (NaN A: always a candidate)
-                  const float u1 = __uint_as_float(mad_hi_u32(x[e], 1u << 23, 0x3F800000u));
-                  cand_f = fmaf(set_gt_f32(u1, __fsub_rd(0x1.fffffep0f, A)),
-                                static_cast<float>(1 << e), cand_f);
-                }
-                uint32_t cand =
-                    __float_as_uint(cand_f + 0x1p23f) & ((1u << SAMPLE_PW) - 1u);
-                // survivors, lowest column first, through one copy of the
-                // exact key (a few per thousand elements); an improvement is
-                // published at once so other threads can skip against it
-                if (__any_sync(0xFFFFFFFFu, cand != 0u)) {
-                  const uint32_t key_before = best_key;
-                  while (cand != 0u) {
-                    const int e = __ffs(cand) - 1;
-                    cand &= cand - 1u;
-                    float ve = v[0];
-                    uint32_t xe = x[0];
+                    for (int e = SAMPLE_BLOCK - 1; e >= 0; --e)
+                      e_star = v[e] != v[e] ? e : e_star;
+                  } else if (!finite) {
+                    key = -INFINITY;
+                  } else {
 #pragma unroll
-                    for (int t = 1; t < SAMPLE_PW; ++t) {
-                      ve = e == t ? v[t] : ve;
-                      xe = e == t ? x[t] : xe;
+                    for (int e = 0; e < SAMPLE_BLOCK; ++e) {
+                      ex[e] = ex2_approx((v[e] - mx) * s1);
+                      sum += ex[e];
                     }
-                    const float key = fmaf(ve, p.inv_tau, gumbel_from_word(xe));
-                    const uint32_t kk = f32_key(key);
-                    const int idx = vb + e;
-                    if (kk > best_key || (kk == best_key && idx < best_idx)) {
+                    key = fmaf(mx, p.inv_tau, __logf(sum)) + gumbel_from_word(xg);
+                  }
+                  const uint32_t kk = f32_key(key);
+                  if (kk >= best_key) {
+                    if (finite) {
+                      // the first entry whose cumulative weight exceeds u * sum
+                      const float uc = __uint_as_float(0x3F800000u | (xc >> 9)) - 0x1.fffffep-1f;
+                      const float target = uc * sum;
+                      float cum = 0.0f;
+                      int hit = -1, last = 0;
+#pragma unroll
+                      for (int e = 0; e < SAMPLE_BLOCK; ++e) {
+                        cum += ex[e];
+                        hit = (hit < 0 && cum > target) ? e : hit;
+                        last = ex[e] > 0.0f ? e : last;
+                      }
+                      e_star = hit >= 0 ? hit : last;
+                    }
+                    const int idx = vb + e_star;
+                    if (kk > best_key || idx < best_idx) {
                       best_key = kk;
                       best_idx = idx;
                       best_val = key;
+                      // published at once so other threads skip against it
+                      if (row_slot)
+                        atomicMax(row_slot,
+                                  (static_cast<unsigned long long>(best_key) << 32) |
+                                      static_cast<unsigned long long>(
+                                          0xFFFFFFFFu - static_cast<uint32_t>(best_idx)));
                     }
                   }
-                  if (best_key != key_before && row_slot)
-                    atomicMax(row_slot,
-                              (static_cast<unsigned long long>(best_key) << 32) |
-                                  static_cast<unsigned long long>(
-                                      0xFFFFFFFFu - static_cast<uint32_t>(best_idx)));
                 }
               }
             } else {

@@ -171,8 +171,10 @@ def dspark_chain_sample(logits, U, V, last_token, draft_tokens, draft_score,
                         K=None, vocab=None, rank=None, stride_n=None,
                         stride_k=None, logits_dtype=None, stream=None,
                         raise_on_error=True) -> int:
-    """dspark_chain_draft with Gumbel-max sampling (probabilistic drafting);
-    seed (uint64), offset (uint32) and temperature as in include/dspark.h."""
+    """dspark_chain_draft drawing each token from softmax(adj / temperature)
+    (probabilistic drafting: a Gumbel-max draw over 16-entry blocks, then the
+    entry inside the block); seed (uint64), offset (uint32) and temperature
+    as in include/dspark.h."""
     import torch
     if logits_dtype is None:
         logits_dtype = BF16 if logits.dtype == torch.bfloat16 else F32
