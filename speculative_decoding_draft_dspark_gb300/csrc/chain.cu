@@ -187,6 +187,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// log2(x) by the hardware approximation (absolute error near 1e-7 for the
+// block sums in [1, 16] it takes)
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // hi32(a * b) + c in one instruction on the FMA pipe
 __device__ __forceinline__ uint32_t mad_hi_u32(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
@@ -550,16 +558,16 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
               // by inverting its cumulative weights with a second uniform.
               // Block j takes words 2 (j % 2) and 2 (j % 2) + 1 of the Philox
               // block with counter (j / 2, n, k, offset): one Philox block
-              // per 32-column chunk.  Since L_j <= max_j / tau + ln 16, a
-              // block can beat the running best only if g_j > best - margin
-              // - max_j / tau - ln 16, i.e. 1 - u < 1 - exp(-A) <= A with
-              // A = exp(max_j / tau + ln 16 - best + margin).  It is skipped
-              // only when u <= 1 - A provably holds (u exact from the word's
-              // mantissa, the bound on it rounded down): one ex2 and no
-              // logarithm per block, the (1 + 2^-10) factor and the margin
-              // covering every rounding and approximation error in A.  Blocks
-              // that pass get their exact key, and their entry when the key
-              // beats the running best.
+              // per 32-column chunk.  Every block's L_j is computed (16 ex2
+              // and one lg2), and the block can beat the running best only
+              // if g_j > best - margin - L_j, i.e. 1 - u < 1 - exp(-A) <= A
+              // with A = exp(L_j - best + margin).  It is skipped only when
+              // u <= 1 - A provably holds (u exact from the word's mantissa,
+              // the bound on it rounded down): one more ex2 and no logarithm
+              // per block, the (1 + 2^-10) factor and the margin covering
+              // every rounding and approximation error in A.  Blocks that
+              // pass get their exact key, and their entry when the key beats
+              // the running best.
               static_assert(SAMPLE_BLOCK == 16, "one 16-column tensor-memory load per block");
               const float s1 = p.inv_tau * 1.4426950408889634f;
               const int vc = v_tile0 + col0;  // a multiple of 32
@@ -611,6 +619,19 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                 float mx = v[0];  // NaN if the block holds one
 #pragma unroll
                 for (int e = 1; e < SAMPLE_BLOCK; ++e) mx = fmax_nan(mx, v[e]);
+                // the block's log partition function, in log2 units: every
+                // block's exact key is one Gumbel away, so the skip test below
+                // is tight (a bound like max / tau + ln 16 passed ten times
+                // more blocks, and their exact keys cost more than this)
+                const float mxs = mx == -INFINITY ? 0.0f : mx;
+                float ex[SAMPLE_BLOCK];
+                float sum = 0.0f;
+#pragma unroll
+                for (int e = 0; e < SAMPLE_BLOCK; ++e) {
+                  ex[e] = ex2_approx((v[e] - mxs) * s1);
+                  sum += ex[e];
+                }
+                const float l2 = fmaf(mxs, s1, lg2_approx(sum));
                 const uint32_t xg = h ? wd[2] : wd[0];  // the block's Gumbel word
                 const uint32_t xc = h ? wd[3] : wd[1];  // the word of its entry
                 // The skip test's threshold: this thread's best or the row's
@@ -623,20 +644,20 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                 const bool none = tkey == 0u || tval != tval;  // nothing to beat yet
                 const float margin = 1e-4f * (1.0f + fabsf(tval));
                 const float s0 = none ? INFINITY
-                                      : (margin - tval) * 1.4426950408889634f + 0x1p-10f + 4.0f;
-                const float A = ex2_approx(fmaf(mx, s1, s0));
-                // u = u1 - (1 - 2^-24) with u1 = 1 + (xg >> 9) 2^-23 (one
-                // mad.hi); u1 <= RD((2 - 2^-23) - A) implies u < 1 - A (NaN A:
-                // always a candidate)
+                                      : (margin - tval) * 1.4426950408889634f + 0x1p-10f;
+                // candidate unless 1 - u >= A = exp(L - best + margin): u = u1 -
+                // (1 - 2^-24) with u1 = 1 + (xg >> 9) 2^-23 (one mad.hi), and
+                // u1 <= RD((2 - 2^-23) - A) implies u < 1 - A (NaN A: always
+                // a candidate)
+                const float A = ex2_approx(l2 + s0);
                 const float u1 = __uint_as_float(mad_hi_u32(xg, 1u << 23, 0x3F800000u));
                 const bool cand = !(u1 <= __fsub_rd(0x1.fffffep0f, A));
                 if (__any_sync(0xFFFFFFFFu, cand) && cand) {
                   // the block's exact key: NaN if it holds a NaN (the first
                   // NaN is then its entry), -inf if nothing in it is finite
-                  float key, sum = 0.0f;
-                  float ex[SAMPLE_BLOCK];
+                  float key;
                   int e_star = 0;
-                  const bool finite = mx == mx && mx != -INFINITY;
+                  const bool finite = mx == mx && sum > 0.0f;
                   if (mx != mx) {
                     key = mx;
 #pragma unroll
@@ -645,12 +666,7 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                   } else if (!finite) {
                     key = -INFINITY;
                   } else {
-#pragma unroll
-                    for (int e = 0; e < SAMPLE_BLOCK; ++e) {
-                      ex[e] = ex2_approx((v[e] - mx) * s1);
-                      sum += ex[e];
-                    }
-                    key = fmaf(mx, p.inv_tau, __logf(sum)) + gumbel_from_word(xg);
+                    key = l2 * 0.6931471805599453f + gumbel_from_word(xg);
                   }
                   const uint32_t kk = f32_key(key);
                   if (kk >= best_key) {
