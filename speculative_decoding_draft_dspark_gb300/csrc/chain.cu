@@ -571,6 +571,10 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
               static_assert(SAMPLE_BLOCK == 16, "one 16-column tensor-memory load per block");
               const float s1 = p.inv_tau * 1.4426950408889634f;
               const int vc = v_tile0 + col0;  // a multiple of 32
+              // the row's shared best, read once per chunk: the Philox rounds
+              // cover its latency
+              const unsigned long long shared_now =
+                  row_slot ? *reinterpret_cast<volatile unsigned long long *>(row_slot) : 0ull;
               uint32_t wd[4];
               philox4x32_10(wd, static_cast<uint32_t>(vc >> 5), prow, pkeys);
 #pragma unroll 1
@@ -608,9 +612,6 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                   }
                 }
                 const int vb = v_tile0 + cb;
-                // the row's shared best (its latency overlaps the block max)
-                const unsigned long long shared_now =
-                    row_slot ? *reinterpret_cast<volatile unsigned long long *>(row_slot) : 0ull;
                 if (vb + SAMPLE_BLOCK > p.vocab) {
 #pragma unroll
                   for (int e = 0; e < SAMPLE_BLOCK; ++e)
@@ -690,7 +691,11 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                       best_idx = idx;
                       best_val = key;
                       // published at once so other threads skip against it
-                      if (row_slot)
+                      // (not a thread's first block of the position: every
+                      // thread has one at the same moment, and those atomics
+                      // on one slot per row cost more than they save; the
+                      // end of the position publishes it anyway)
+                      if (row_slot && !none)
                         atomicMax(row_slot,
                                   (static_cast<unsigned long long>(best_key) << 32) |
                                       static_cast<unsigned long long>(
