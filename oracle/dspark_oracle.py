@@ -172,11 +172,14 @@ def _block_log_partition(b: np.ndarray) -> np.ndarray:
 
 def _within_block(b: np.ndarray, u: float) -> int:
     """The entry of one block drawn with u in (0, 1): the first NaN entry if
-    there is one, the first entry if all are -inf, else the first e with
+    there is one, else the first +inf entry if there is one (it holds all
+    the weight), the first entry if all are -inf, else the first e with
     sum_{i <= e} exp(b_i - max) > u * sum_i exp(b_i - max)."""
     if np.isnan(b).any():
         return int(np.argmax(np.isnan(b)))
     m = np.max(b)
+    if m == np.inf:
+        return int(np.argmax(b == np.inf))
     if m == -np.inf:
         return 0
     c = np.cumsum(np.exp(b - m))

@@ -558,13 +558,13 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
               // by inverting its cumulative weights with a second uniform.
               // Block j takes words 2 (j % 2) and 2 (j % 2) + 1 of the Philox
               // block with counter (j / 2, n, k, offset): one Philox block
-              // per 32-column chunk.  Every block's L_j is computed (16 ex2
-              // and one lg2), and the block can beat the running best only
+              // per 32-column chunk.  A block can beat the running best only
               // if g_j > best - margin - L_j, i.e. 1 - u < 1 - exp(-A) <= A
-              // with A = exp(L_j - best + margin).  It is skipped only when
-              // u <= 1 - A provably holds (u exact from the word's mantissa,
-              // the bound on it rounded down): one more ex2 and no logarithm
-              // per block, the (1 + 2^-10) factor and the margin covering
+              // with A = exp(L_j - best + margin), computed for every block
+              // from its weights relative to the best (16 ex2, no
+              // logarithm).  It is skipped only when u <= 1 - A provably
+              // holds (u exact from the word's mantissa, the bound on it
+              // rounded down), the (1 + 2^-10) factor and the margin covering
               // every rounding and approximation error in A.  Blocks that
               // pass get their exact key, and their entry when the key beats
               // the running best.
@@ -617,22 +617,6 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                   for (int e = 0; e < SAMPLE_BLOCK; ++e)
                     if (vb + e >= p.vocab) v[e] = -INFINITY;
                 }
-                float mx = v[0];  // NaN if the block holds one
-#pragma unroll
-                for (int e = 1; e < SAMPLE_BLOCK; ++e) mx = fmax_nan(mx, v[e]);
-                // the block's log partition function, in log2 units: every
-                // block's exact key is one Gumbel away, so the skip test below
-                // is tight (a bound like max / tau + ln 16 passed ten times
-                // more blocks, and their exact keys cost more than this)
-                const float mxs = mx == -INFINITY ? 0.0f : mx;
-                float ex[SAMPLE_BLOCK];
-                float sum = 0.0f;
-#pragma unroll
-                for (int e = 0; e < SAMPLE_BLOCK; ++e) {
-                  ex[e] = ex2_approx((v[e] - mxs) * s1);
-                  sum += ex[e];
-                }
-                const float l2 = fmaf(mxs, s1, lg2_approx(sum));
                 const uint32_t xg = h ? wd[2] : wd[0];  // the block's Gumbel word
                 const uint32_t xc = h ? wd[3] : wd[1];  // the word of its entry
                 // The skip test's threshold: this thread's best or the row's
@@ -644,30 +628,53 @@ __global__ void __launch_bounds__(chain_threads(EPI), 1)
                 const float tval = tkey == best_key ? best_val : f32_from_key(tkey);
                 const bool none = tkey == 0u || tval != tval;  // nothing to beat yet
                 const float margin = 1e-4f * (1.0f + fabsf(tval));
-                const float s0 = none ? INFINITY
-                                      : (margin - tval) * 1.4426950408889634f + 0x1p-10f;
-                // candidate unless 1 - u >= A = exp(L - best + margin): u = u1 -
-                // (1 - 2^-24) with u1 = 1 + (xg >> 9) 2^-23 (one mad.hi), and
-                // u1 <= RD((2 - 2^-23) - A) implies u < 1 - A (NaN A: always
-                // a candidate)
-                const float A = ex2_approx(l2 + s0);
+                // The block's weight relative to the threshold, rel = sum of
+                // exp(adj / tau - best), so that exp(L_j - best) = rel: every
+                // block's exact key is one Gumbel away and the test below is
+                // tight, with no max shift and no logarithm.  An entry 126
+                // octaves below the threshold flushes to zero (its block
+                // could not win by any Gumbel value); one that would overflow
+                // makes the block a candidate, whose exact key is computed
+                // with the max shift.
+                const float c2 = none ? 0.0f : tval * 1.4426950408889634f;
+                float rel = 0.0f;
+#pragma unroll
+                for (int e = 0; e < SAMPLE_BLOCK; ++e) rel += ex2_approx(fmaf(v[e], s1, -c2));
+                // candidate unless 1 - u >= A = exp(L_j - best + margin) =
+                // rel e^margin (times 2^(2^-10) for the approximations): u =
+                // u1 - (1 - 2^-24) with u1 = 1 + (xg >> 9) 2^-23 (one mad.hi),
+                // and u1 <= RD((2 - 2^-23) - A) implies u < 1 - A (NaN A:
+                // always a candidate)
+                const float A =
+                    none ? INFINITY
+                         : rel * ex2_approx(fmaf(margin, 1.4426950408889634f, 0x1p-10f));
                 const float u1 = __uint_as_float(mad_hi_u32(xg, 1u << 23, 0x3F800000u));
                 const bool cand = !(u1 <= __fsub_rd(0x1.fffffep0f, A));
                 if (__any_sync(0xFFFFFFFFu, cand) && cand) {
-                  // the block's exact key: NaN if it holds a NaN (the first
-                  // NaN is then its entry), -inf if nothing in it is finite
-                  float key;
+                  // the block's exact key, max-shifted: NaN if it holds a NaN
+                  // (the first NaN is then its entry), +inf if it holds +inf
+                  // (the first one is its entry), -inf if nothing is finite
+                  float mx = v[0];
+#pragma unroll
+                  for (int e = 1; e < SAMPLE_BLOCK; ++e) mx = fmax_nan(mx, v[e]);
+                  float key, sum = 0.0f;
+                  float ex[SAMPLE_BLOCK];
                   int e_star = 0;
-                  const bool finite = mx == mx && sum > 0.0f;
-                  if (mx != mx) {
+                  const bool finite = mx == mx && fabsf(mx) != INFINITY;
+                  if (!finite) {
                     key = mx;
 #pragma unroll
                     for (int e = SAMPLE_BLOCK - 1; e >= 0; --e)
-                      e_star = v[e] != v[e] ? e : e_star;
-                  } else if (!finite) {
-                    key = -INFINITY;
+                      e_star = (v[e] != v[e] || v[e] == mx) ? e : e_star;
+                    if (mx == -INFINITY) e_star = 0;
                   } else {
-                    key = l2 * 0.6931471805599453f + gumbel_from_word(xg);
+#pragma unroll
+                    for (int e = 0; e < SAMPLE_BLOCK; ++e) {
+                      ex[e] = ex2_approx((v[e] - mx) * s1);
+                      sum += ex[e];
+                    }
+                    key = fmaf(mx, p.inv_tau, lg2_approx(sum) * 0.6931471805599453f) +
+                          gumbel_from_word(xg);
                   }
                   const uint32_t kk = f32_key(key);
                   if (kk >= best_key) {

@@ -208,6 +208,9 @@ def _score_ok(got, want, floor=1e-3):
     if np.isnan(want):
         assert np.isnan(got)
         return
+    if np.isinf(want):
+        assert got == want, (got, want)
+        return
     assert abs(float(got) - want) <= SCORE_RTOL * max(abs(want), floor), (got, want)
 
 

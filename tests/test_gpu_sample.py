@@ -166,9 +166,11 @@ def test_nan_row_and_bad_last_token():
     logits, U, V, last = _inputs(8, 3, 1024, 32, "f32", seed=9)
     logits[1, 0, 500] = np.nan
     logits[1, 0, 100] = np.nan          # first NaN wins over any noise
+    logits[5, 1, 700] = np.inf
+    logits[5, 1, 333] = np.inf          # the first +inf holds all the weight
     last[3] = 5000                      # out of range -> 0
     got, score, st = run_chain(logits, "f32", U, V, last, sample=SM)
-    assert got[1, 0] == 100
+    assert got[1, 0] == 100 and got[5, 1] == 333
     assert st & D.DEV_NAN_LOGIT and st & D.DEV_TOKEN_OOR
     last_ref = last.copy()
     last_ref[3] = 0

@@ -9,7 +9,7 @@ published known-answer vectors.  The sampling rule is pinned by its
 distribution (chi-square against the softmax over several blocks, a
 ragged last block included), with planted mistakes in each of its steps
 failing that pin; by closed forms (one block of equal entries, blocks with
-one finite entry, NaN and -inf rows); by its zero-temperature limit (the
+one finite entry, NaN and infinite rows); by its zero-temperature limit (the
 greedy oracle) and by a chain whose bias forces the next token.
 """
 import json
@@ -146,16 +146,19 @@ def test_blocks_with_one_finite_entry_reduce_to_gumbel_max():
     assert r["margin"][0] == top2[1] - top2[0]
 
 
-def test_nan_and_minus_infinity_rows():
-    adj = np.random.default_rng(1).standard_normal((3, 50))
+def test_nan_and_infinite_rows():
+    adj = np.random.default_rng(1).standard_normal((4, 50))
     adj[0, 20] = np.nan
     adj[0, 3] = np.nan           # the first NaN wins, whatever the noise
     adj[1, :] = -np.inf          # nothing finite: the first entry
     adj[2, 40:] = -np.inf        # a ragged, partly -inf last block
-    r = oracle.sample_position(adj, 1.0, 5, 0, [0, 1, 2], 0)
+    adj[3, 37] = np.inf
+    adj[3, 21] = np.inf          # the first +inf holds all the weight
+    r = oracle.sample_position(adj, 1.0, 5, 0, [0, 1, 2, 3], 0)
     assert r["tok"][0] == 3 and np.isnan(r["score"][0])
     assert r["tok"][1] == 0 and r["score"][1] == -np.inf
     assert r["tok"][2] < 40
+    assert r["tok"][3] == 21 and r["score"][3] == np.inf
 
 
 def _factors(vocab, rank):
