@@ -43,7 +43,8 @@
 //               quarter w % 4; the warps of a quarter split each tile's
 //               32-column chunks; they also decode the winners and, with a
 //               single tile per position, gather half of each U row);
-//               sampling runs warps 8-15
+//               sampling runs warps 8-19 with full request tiles, and only
+//               warps 4-11 when the tile holds its requests several times
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
@@ -71,13 +72,15 @@ constexpr int SMEM_USED = SMEM_BAR_OFF + NUM_BARS * 8 + 16;
 constexpr int CHAIN_SMEM_BYTES = SMEM_USED + 1024;  // 1 KB alignment slack
 // warps 0-3 have fixed roles; EPI epilogue warps follow: 8 for the argmax
 // chain (4 / 8 / 12 measured at the headline: chain 311 / 295 / 301 us;
-// Stress 2410 / 2176 / 2157 us), 12 for sampling, whose epilogue does far
-// more arithmetic per element (12 / 16 / 20 / 24 warps with 16-column
-// pieces: 697 / 732 / 737 / 767 us at the headline; more warps leave fewer
-// registers per thread)
+// Stress 2410 / 2176 / 2157 us); for sampling, whose epilogue does more
+// arithmetic per element, 16 with full request tiles and 8 when requests
+// are held several times (8 / 12 / 16 / 20 warps: headline 499 / 433 / 421
+// / 440 us, Conc-64 234 / 245 / 263 / 286 us, Gemma4-12B 191 / 203 / 212 /
+// 233 us)
 constexpr int chain_threads(int epi) { return (4 + epi) * 32; }
 constexpr int EPI_ARGMAX = 8;
-constexpr int EPI_SAMPLE = 12;
+constexpr int EPI_SAMPLE = 16;      // sampling, full request tiles
+constexpr int EPI_SAMPLE_REP = 8;   // sampling, requests held 2 or 4 times
 constexpr int SAMPLE_BLOCK = 16;  // vocabulary entries per block of the sampling draw
 constexpr uint32_t TMEM_COLS = 512;  // two 256-column fp32 accumulators
 // bytes of V worth protecting in L2 across positions (measured on GB300:
@@ -851,11 +854,11 @@ static cudaError_t ensure_kernel_attrs(int dev) {
   if (g_attr_done[dev]) return cudaSuccess;
   cudaError_t e;
   if ((e = set_smem_attr<DSPARK_BF16, true, EPI_SAMPLE, 1>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<DSPARK_BF16, true, EPI_SAMPLE, 2>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<DSPARK_BF16, true, EPI_SAMPLE, 4>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<DSPARK_BF16, true, EPI_SAMPLE_REP, 2>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<DSPARK_BF16, true, EPI_SAMPLE_REP, 4>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<DSPARK_F32, true, EPI_SAMPLE, 1>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<DSPARK_F32, true, EPI_SAMPLE, 2>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<DSPARK_F32, true, EPI_SAMPLE, 4>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<DSPARK_F32, true, EPI_SAMPLE_REP, 2>()) != cudaSuccess) return e;
+  if ((e = set_smem_attr<DSPARK_F32, true, EPI_SAMPLE_REP, 4>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<DSPARK_BF16, false, EPI_ARGMAX, 1>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<DSPARK_F32, false, EPI_ARGMAX, 1>()) != cudaSuccess) return e;
   g_attr_done[dev] = true;
@@ -970,7 +973,11 @@ dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream) {
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(chain_threads(a.sample ? EPI_SAMPLE : EPI_ARGMAX));
+  // sampling a batch of at most 32 (64) requests: every request four
+  // (two) times in the tile's rows
+  const int rep = a.sample ? (a.N <= 32 ? 4 : a.N <= 64 ? 2 : 1) : 1;
+  cfg.blockDim = dim3(chain_threads(!a.sample ? EPI_ARGMAX
+                                    : rep == 1 ? EPI_SAMPLE : EPI_SAMPLE_REP));
   cfg.dynamicSmemBytes = CHAIN_SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -982,17 +989,14 @@ dspark_status chain_draft_launch(const ChainArgs &a, cudaStream_t stream) {
   // QPT quanta
   const bool one_tile = (n_quanta + n_vgroups - 1) / n_vgroups <= QPT;
   cudaError_t e;
-  // sampling a batch of at most 32 (64) requests: every request four
-  // (two) times in the tile's rows
-  const int rep = a.sample ? (a.N <= 32 ? 4 : a.N <= 64 ? 2 : 1) : 1;
 #define DSPARK_LAUNCH(LDT, S, E, R)                                                   \
   e = one_tile ? cudaLaunchKernelEx(&cfg, chain_kernel<LDT, S, E, true, R>, tmV, tmL, p) \
                : cudaLaunchKernelEx(&cfg, chain_kernel<LDT, S, E, false, R>, tmV, tmL, p)
 #define DSPARK_LAUNCH_REP(LDT)                 \
   if (rep == 4)                                \
-    DSPARK_LAUNCH(LDT, true, EPI_SAMPLE, 4);   \
+    DSPARK_LAUNCH(LDT, true, EPI_SAMPLE_REP, 4); \
   else if (rep == 2)                           \
-    DSPARK_LAUNCH(LDT, true, EPI_SAMPLE, 2);   \
+    DSPARK_LAUNCH(LDT, true, EPI_SAMPLE_REP, 2); \
   else                                         \
     DSPARK_LAUNCH(LDT, true, EPI_SAMPLE, 1)
   if (a.sample) {
