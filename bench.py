@@ -697,8 +697,9 @@ def run_stale_select(st, cfg, stream, iters=200):
 
 def run_sample_chain(st, cfg, stream, iters=50):
     """Probabilistic drafting (not part of the metric): dspark_chain_sample
-    (Gumbel-max with Philox4x32-10 noise) against dspark_chain_draft on the
-    same inputs, back-to-back launches timed with CUDA events."""
+    (a Gumbel-max draw over 16-entry blocks with Philox4x32-10 words, then
+    the entry inside the block) against dspark_chain_draft on the same
+    inputs, back-to-back launches timed with CUDA events."""
     import torch
     D = st.D
 
@@ -725,11 +726,11 @@ def run_sample_chain(st, cfg, stream, iters=50):
     elems = cfg.N * cfg.K * cfg.vocab
     out["elements"] = elems
     out["gelem_per_s"] = round(elems / (out["sample_us"] * 1e-6) / 1e9, 2)
-    # Issue roofline: the path is bound by instruction issue (Philox words,
-    # the skip test), so the work is the warp instructions one launch issues,
+    # Issue roofline: the work is the warp instructions one launch issues,
     # measured by ncu (smsp__inst_executed.sum, recorded with the kernel
     # source's hash), and the peak is four warp instructions per SM per clock
-    # at the 2070 MHz maximum SM clock
+    # at the 2070 MHz maximum SM clock.  The launch also moves the greedy
+    # chain's bytes (logits once, V once), reported against HBM beside it.
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     peak = sms * 4 * 2.070e9 / 1e12
     inst = (_recorded(SAMPLE_PROFILE, "warp_instructions_per_launch")
@@ -741,7 +742,10 @@ def run_sample_chain(st, cfg, stream, iters=50):
                        "warp_instructions_per_launch": inst,
                        "thread_instructions_per_element":
                            None if inst is None else round(inst * 32 / elems, 2),
-                       "peak_source": "derived: SMs x 4 issue slots x 2070 MHz"}
+                       "peak_source": "derived: SMs x 4 issue slots x 2070 MHz",
+                       "frac_hbm": round(algorithmic_bytes_per_launch(cfg)
+                                         / (out["sample_us"] * 1e-6) / 1e9
+                                         / measured_peaks()[0], 4)}
     out["note"] = ("dspark_chain_sample vs dspark_chain_draft, back-to-back "
                    "launches; not part of the step metric")
     return out
