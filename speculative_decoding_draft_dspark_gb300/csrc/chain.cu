@@ -205,13 +205,6 @@ __device__ __forceinline__ uint32_t mad_hi_u32(uint32_t a, uint32_t b, uint32_t 
   return d;
 }
 
-// 1.0f if a > b or either is NaN (unordered), else 0.0f
-__device__ __forceinline__ float set_gt_f32(float a, float b) {
-  float d;
-  asm("set.gtu.f32.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
-  return d;
-}
-
 // Gumbel noise from one 32-bit word: u = (2 (x >> 9) + 1) 2^-24 (exact: the
 // mantissa trick gives 1 + (x >> 9) 2^-23, and subtracting 1 - 2^-24 is exact
 // by Sterbenz's lemma), g = -ln(-ln u).  The inner ln is the accurate logf,
