@@ -206,46 +206,106 @@ __device__ __forceinline__ Acc128 to_fixed128(double s, int e_max) {
   return r;
 }
 
-// a * 2^u rounded to the nearest double, ties to even
-__device__ __forceinline__ double from_fixed128(const Acc128 &a, int e_max) {
+// (hi:lo) * 2^u rounded to the nearest double, ties to even: the bit
+// pattern of the non-negative, finite result (no caller comes near the
+// overflow threshold)
+__device__ __forceinline__ unsigned long long round_u128_to_f64(unsigned long long lo,
+                                                               unsigned long long hi,
+                                                               int u) {
   int h;
-  if (a.hi)
-    h = 64 + 63 - __clzll(static_cast<long long>(a.hi));
-  else if (a.lo)
-    h = 63 - __clzll(static_cast<long long>(a.lo));
+  if (hi)
+    h = 64 + 63 - __clzll(static_cast<long long>(hi));
+  else if (lo)
+    h = 63 - __clzll(static_cast<long long>(lo));
   else
-    return 0.0;
-  const int u = e_max - 1075 - kFixG128;
-  int rb = h - 52;
-  const int rb_sub = -1074 - u;
+    return 0ull;
+  int rb = h - 52;                 // lowest bit a 53-bit significand keeps
+  const int rb_sub = -1074 - u;    // lowest bit a subnormal keeps
   if (rb < rb_sub) rb = rb_sub;
-  // the whole value fits (a < 2^53): exact.  (Not reached from the scan,
-  // whose nonzero sums have their top bit at kFixG128 + 52 or above.)
-  if (rb <= 0) return ldexp(static_cast<double>(a.lo), u);
-  unsigned long long mant =
-      rb >= 64 ? a.hi >> (rb - 64) : (a.lo >> rb) | (a.hi << (64 - rb));
-  mant &= (1ull << 53) - 1ull;
-  const int pos = rb - 1;  // the round bit
-  bool round, sticky;
-  if (pos >= 64) {
-    round = (a.hi >> (pos - 64)) & 1ull;
-    sticky = a.lo != 0ull || (a.hi & ((1ull << (pos - 64)) - 1ull)) != 0ull;
+  unsigned long long mant;
+  if (rb <= 0) {
+    mant = lo << (-rb);            // the whole value fits (< 2^53): exact
   } else {
-    round = (a.lo >> pos) & 1ull;
-    sticky = pos > 0 && (a.lo & ((1ull << pos) - 1ull)) != 0ull;
+    if (rb > h + 1) return 0ull;   // below half the smallest subnormal
+    mant = rb >= 64 ? hi >> (rb - 64) : (lo >> rb) | (hi << (64 - rb));
+    mant &= (1ull << 53) - 1ull;
+    const int pos = rb - 1;        // the round bit
+    bool round, sticky;
+    if (pos >= 64) {
+      round = (hi >> (pos - 64)) & 1ull;
+      sticky = lo != 0ull || (hi & ((1ull << (pos - 64)) - 1ull)) != 0ull;
+    } else {
+      round = (lo >> pos) & 1ull;
+      sticky = pos > 0 && (lo & ((1ull << pos) - 1ull)) != 0ull;
+    }
+    if (round && (sticky || (mant & 1ull))) mant += 1ull;
   }
-  if (round && (sticky || (mant & 1ull))) mant += 1ull;
-  int e2 = rb + u;
+  int e2 = rb + u;                 // value = mant * 2^e2
   if (mant == (1ull << 53)) {
     mant >>= 1;
     e2 += 1;
   }
-  const unsigned long long bits =
-      mant >= (1ull << 52)
-          ? (static_cast<unsigned long long>(e2 + 52 + 1023) << 52) |
-                (mant & ((1ull << 52) - 1ull))
-          : mant;  // subnormal, e2 == -1074
+  return mant >= (1ull << 52)
+             ? (static_cast<unsigned long long>(e2 + 52 + 1023) << 52) |
+                   (mant & ((1ull << 52) - 1ull))
+             : mant;  // subnormal, e2 == -1074
+}
+
+// a * 2^u rounded to the nearest double, ties to even
+__device__ __forceinline__ double from_fixed128(const Acc128 &a, int e_max) {
+  return __longlong_as_double(static_cast<long long>(
+      round_u128_to_f64(a.lo, a.hi, e_max - 1075 - kFixG128)));
+}
+
+// ------------------------------------------------------------------------
+// Conversions between fp32 and fp64 in integer arithmetic, exact (IEEE,
+// ties to even): the fp64 pipe of this part issues about one warp
+// instruction per 64 cycles of an SM sub-partition, conversions included,
+// so the survival loop keeps only its multiply there (a 15-position batch
+// of 1024 requests: 16.5 us with the conversions on the fp64 pipe, 9.5 us
+// without).  An integer form of the multiply measured slower than the pipe.
+// ------------------------------------------------------------------------
+// batches from this many slots take the integer conversions
+constexpr int kIntCvtMinSlots = 4096;
+
+// c as a double, for c a non-negative finite float
+__device__ __forceinline__ double f32_to_f64(float c) {
+  const uint32_t b = __float_as_uint(c);
+  const uint32_t e = b >> 23;  // sign 0
+  uint32_t m = b & 0x7FFFFFu;
+  unsigned long long bits;
+  if (e != 0) {
+    bits = (static_cast<unsigned long long>(e + 896u) << 52) |
+           (static_cast<unsigned long long>(m) << 29);
+  } else if (m != 0) {           // subnormal: normalise the significand
+    const int sh = __clz(m) - 8;  // brings the top bit to bit 23
+    m <<= sh;
+    bits = (static_cast<unsigned long long>(897 - sh) << 52) |
+           (static_cast<unsigned long long>(m & 0x7FFFFFu) << 29);
+  } else {
+    bits = 0ull;
+  }
   return __longlong_as_double(static_cast<long long>(bits));
+}
+
+// d rounded to the nearest float, for d a non-negative double below 2^127
+__device__ __forceinline__ float f64_to_f32_rn(double d) {
+  const unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(d));
+  const int e = static_cast<int>(b >> 52);  // sign 0
+  if (e == 0) return 0.0f;  // fp64 subnormals lie far below half an fp32 one
+  const unsigned long long m = (b & ((1ull << 52) - 1ull)) | (1ull << 52);
+  const int e32 = e - 1023 + 127;  // biased fp32 exponent of a normal result
+  const int sh = e32 >= 1 ? 29 : 29 + 1 - e32;  // bits dropped from m
+  if (sh > 54) return 0.0f;
+  unsigned long long q = m >> sh;
+  const bool round = (m >> (sh - 1)) & 1ull;
+  const bool sticky = (m & ((1ull << (sh - 1)) - 1ull)) != 0ull;
+  if (round && (sticky || (q & 1ull))) q += 1ull;
+  // normal: q in [2^23, 2^24], a carry lands in the exponent (up to 2^127
+  // at most); subnormal: q below 2^23, or 2^23 for the smallest normal
+  const uint32_t bits = e32 >= 1 ? (static_cast<uint32_t>(e32 - 1) << 23) + static_cast<uint32_t>(q)
+                                 : static_cast<uint32_t>(q);
+  return __uint_as_float(bits);
 }
 
 // ------------------------------------------------------------------------
@@ -287,6 +347,19 @@ struct OpMinNan {
     return d;
   }
 };
+// two running maxima scanned together
+struct MaxPair {
+  float pre, run;
+};
+__device__ __forceinline__ MaxPair shfl_up(const MaxPair &v, int o) {
+  return MaxPair{__shfl_up_sync(FULL, v.pre, o), __shfl_up_sync(FULL, v.run, o)};
+}
+struct OpMaxPair {
+  __device__ MaxPair operator()(const MaxPair &a, const MaxPair &b) const {
+    return MaxPair{fmax_nan(a.pre, b.pre), fmax_nan(a.run, b.run)};
+  }
+};
+
 struct OpAcc {
   __device__ Acc256 operator()(Acc256 a, const Acc256 &b) const {
     acc_add(a, b);
@@ -466,19 +539,17 @@ __device__ __forceinline__ double f64_from_key(unsigned long long k) {
 }
 
 // ------------------------------------------------------------------------
-// global priority order (larger key first, then smaller slot) of NK slots.
-// Each warp first sorts segments of 128 slots in registers (a bitonic
-// network, below); then level l merges neighbouring runs of 128 * 2^l
-// (merge path): every thread writes ceil(NK / blockDim), at least four,
-// consecutive outputs, finding how many of them come from the left run by a
-// binary search (the co-rank) and then merging sequentially.  Only 16-bit
-// slot ids move (between sidx and stmp); keys stay indexed by slot.
-// n log2(n / 128) merge steps in log2(NK / 128) levels, against
-// n log2(n)^2 / 4 compare-exchanges in about log2(n)^2 / 2 stages for a
-// sorting network over the whole array.  (The requests' own runs of K
-// arrive sorted, since a survival never increases along a request, but the
-// segments subsume them.)  On return sidx[0 .. NK) is the order and
-// keys[0 .. NK) the keys in that order.
+// global priority order (larger key first, then smaller slot) of NK slots,
+// on the fp64 keys: the requests' runs of K arrive sorted (a survival never
+// increases along a request), and level l merges neighbouring runs of
+// K * 2^l (merge path): every thread writes ceil(NK / blockDim), at least
+// four, consecutive outputs, finding how many of them come from the left
+// run by a binary search (the co-rank) and then merging sequentially.  Only
+// 16-bit slot ids move (between sidx and stmp); keys stay indexed by slot.
+// n log2(n / K) merge steps in log2(NK / K) levels.  On return sidx[0 ..
+// NK) is the order and keys[0 .. NK) the keys in that order.  Batches of
+// more than 4096 slots take this path; smaller ones only when the fast
+// order below finds two survivals it cannot tell apart.
 // ------------------------------------------------------------------------
 __device__ __forceinline__ bool prio_first(unsigned long long ka, uint32_t sa,
                                            unsigned long long kb, uint32_t sb) {
@@ -490,79 +561,6 @@ constexpr int kMaxPerThread = (kMaxSlots + SEL_THREADS - 1) / SEL_THREADS;
 // fewer co-rank searches, which bound a level (random key reads)
 constexpr int kMergeMinOut = 4;
 
-// Before the merge: each warp sorts segments of 32 * kSegPerLane slots in
-// registers with a bitonic network (lane l holds elements l * E .. l * E +
-// E - 1 of the segment; strides of E or more exchange with another lane by
-// shuffle, shorter ones inside the lane), so the merge starts from runs of
-// 32 * E instead of K.  Every segment is sorted in priority order (the
-// direction bit is taken from the index inside the segment); the slots past
-// NK of the last segment are sentinels (key 0, slot 0xFFFF) that sort last
-// and are not written back.
-constexpr int kSegPerLane = 4;
-constexpr int kSegLen = 32 * kSegPerLane;
-// the network costs n log2(seg)^2 / 4 instructions' worth of exchanges: it
-// pays for small batches only; larger ones merge the requests' runs of K
-constexpr int kWarpSortMaxNK = 4096;
-
-__device__ void warp_sort_segments(const unsigned long long *keys, uint16_t *sidx,
-                                   const int NK) {
-  constexpr int E = kSegPerLane;
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int nwarps = blockDim.x >> 5;
-  for (int base = warp * kSegLen; base < NK; base += nwarps * kSegLen) {
-    unsigned long long k[E];
-    uint32_t v[E];
-#pragma unroll
-    for (int j = 0; j < E; ++j) {
-      const int i = base + lane * E + j;
-      k[j] = i < NK ? keys[i] : 0ull;
-      v[j] = i < NK ? static_cast<uint32_t>(i) : 0xFFFFu;
-    }
-#pragma unroll
-    for (int s = 2; s <= kSegLen; s <<= 1) {
-#pragma unroll
-      for (int d = s >> 1; d >= E; d >>= 1) {  // partner in another lane
-        const int m = d / E;
-        const bool lower = (lane & m) == 0;
-#pragma unroll
-        for (int j = 0; j < E; ++j) {
-          const int i = lane * E + j;
-          const unsigned long long pk = __shfl_xor_sync(0xFFFFFFFFu, k[j], m);
-          const uint32_t pv = __shfl_xor_sync(0xFFFFFFFFu, v[j], m);
-          if ((lower == ((i & s) == 0)) != prio_first(k[j], v[j], pk, pv)) {
-            k[j] = pk;
-            v[j] = pv;
-          }
-        }
-      }
-#pragma unroll
-      for (int dd = E / 2; dd >= 1; dd >>= 1) {  // partner in this lane
-        if (dd >= s) continue;
-#pragma unroll
-        for (int j = 0; j < E; ++j) {
-          if (j & dd) continue;
-          const int jj = j | dd;
-          const bool up = ((lane * E + j) & s) == 0;
-          if (up != prio_first(k[j], v[j], k[jj], v[jj])) {
-            const unsigned long long tk = k[j];
-            const uint32_t tv = v[j];
-            k[j] = k[jj];
-            v[j] = v[jj];
-            k[jj] = tk;
-            v[jj] = tv;
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < E; ++j) {
-      const int i = base + lane * E + j;
-      if (i < NK) sidx[i] = static_cast<uint16_t>(v[j]);
-    }
-  }
-}
-
 __device__ void block_merge_runs(unsigned long long *keys, uint16_t *sidx,
                                  uint16_t *stmp, const int NK, const int K) {
   const int tid = threadIdx.x;
@@ -572,15 +570,10 @@ __device__ void block_merge_runs(unsigned long long *keys, uint16_t *sidx,
   const int Cm = max(C, kMergeMinOut);  // merge levels: outputs per thread
   const int m0 = min(NK, tid * Cm), m1 = min(NK, m0 + Cm);
   uint16_t *src = sidx, *dst = stmp;
-  const bool segments = NK <= kWarpSortMaxNK;
   __syncthreads();  // the keys are in place
-  if (segments) {
-    warp_sort_segments(keys, sidx, NK);
-  } else {
-    for (int i = tid; i < NK; i += NT) sidx[i] = static_cast<uint16_t>(i);
-  }
+  for (int i = tid; i < NK; i += NT) sidx[i] = static_cast<uint16_t>(i);
   __syncthreads();
-  for (int L = segments ? kSegLen : K; L < NK; L <<= 1) {
+  for (int L = K; L < NK; L <<= 1) {
     int p = m0;
     while (p < m1) {
       // the pair of runs [base, base + L) and [base + L, base + 2L) holding p
@@ -826,17 +819,19 @@ __device__ bool fast_order(unsigned long long *keys, uint16_t *sidx,
 // ------------------------------------------------------------------------
 constexpr int kMaxChunk = (kMaxSlots + 1 + SEL_THREADS - 1) / SEL_THREADS + 1;
 
-// Survival products of `conf` (fp64, left to right, clamped), sort keys
-// (bits(s) + 1, 0 for non-sampling requests) and the merged order.  With
-// `outputs`, writes survival, sorted_slots, n_eligible and n_sampling.
-__device__ void survival_order(const SelectArgs &a, const float *conf,
-                               const bool outputs, unsigned long long *keys,
-                               uint16_t *sidx, uint16_t *stmp,
-                               unsigned long long *sortbuf, int *sh_int, int &n_s,
-                               uint32_t &st, const int T_pf) {
+// Survival products of `conf` (fp64, left to right, clamped) and sort keys
+// (bits(s) + 1, 0 for non-sampling requests), by slot; returns this
+// thread's count of sampling requests.  kIntCvt: the fp32 <-> fp64
+// conversions in integer arithmetic, which pays once the fp64 pipe is the
+// bound (thousands of slots); small batches wait on the longer dependent
+// chain instead, and keep the pipe's conversions.
+template <bool kIntCvt>
+__device__ __forceinline__ int survival_products(const SelectArgs &a, const float *conf,
+                                                 const bool outputs,
+                                                 unsigned long long *keys, uint32_t &st) {
   const int tid = threadIdx.x;
   const int NT = blockDim.x;
-  const int N = a.N, K = a.K, NK = N * K;
+  const int N = a.N, K = a.K;
   int my_ns = 0;
   constexpr int KG = 8;  // confidences loaded together (one memory round trip)
   for (int n = tid; n < N; n += NT) {
@@ -858,24 +853,43 @@ __device__ void survival_order(const SelectArgs &a, const float *conf,
           c = (c > 1.0f) ? 1.0f : 0.0f;  // NaN and negatives -> 0
         }
         if (c == 0.0f) c = 0.0f;  // -0 -> +0: sort keys are bit patterns
-        prod = __dmul_rn(prod, static_cast<double>(c));
+        prod = __dmul_rn(prod, kIntCvt ? f32_to_f64(c) : static_cast<double>(c));
         if (outputs && a.survival)
           a.survival[static_cast<size_t>(n) * K + k] =
-              samp ? __double2float_rn(prod) : 0.0f;
+              samp ? (kIntCvt ? f64_to_f32_rn(prod) : __double2float_rn(prod)) : 0.0f;
         keys[n * K + k] =
             samp ? static_cast<unsigned long long>(__double_as_longlong(prod)) + 1ull
                  : 0ull;
       }
     }
   }
+  return my_ns;
+}
+
+// Survival products of `conf` (fp64, left to right, clamped), sort keys
+// (bits(s) + 1, 0 for non-sampling requests) and the merged order.  With
+// `outputs`, writes survival, sorted_slots, n_eligible and n_sampling.
+__device__ void survival_order(const SelectArgs &a, const float *conf,
+                               const bool outputs, unsigned long long *keys,
+                               uint16_t *sidx, uint16_t *stmp,
+                               unsigned long long *sortbuf, int *sh_int, int &n_s,
+                               uint32_t &st, const int T_pf) {
+  const int tid = threadIdx.x;
+  const int NT = blockDim.x;
+  const int N = a.N, K = a.K, NK = N * K;
+  const int my_ns = NK >= kIntCvtMinSlots
+                        ? survival_products<true>(a, conf, outputs, keys, st)
+                        : survival_products<false>(a, conf, outputs, keys, st);
   n_s = block_reduce(my_ns, OpAddInt(), 0, sh_int);
   const int S = n_s * K;
-  // the budget's cost slice into L1 (one 128-byte line per thread) while the
-  // order is built
+  // the cost entries the budget reads into L1 (128-byte lines) while the
+  // order is built: cost[T .. T + S], and with forcing also the entries
+  // before T (running max) or after T + S (suffix minimum)
   if (T_pf >= 0 && T_pf < a.L) {
-    const int hi = min(a.L, T_pf + S + 1);
-    const int line = (T_pf >> 5) + tid;  // 32 floats per line
-    if (line * 32 < hi) asm volatile("prefetch.global.L1 [%0];" ::"l"(a.cost + line * 32));
+    const int lo = (a.flags & DSPARK_COST_FORCE_MONOTONE) ? 0 : T_pf;
+    const int hi = (a.flags & DSPARK_COST_FORCE_SUFFIX_MIN) ? a.L : min(a.L, T_pf + S + 1);
+    for (int line = (lo >> 5) + tid; line * 32 < hi; line += NT)  // 32 floats a line
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(a.cost + line * 32));
   }
 
   bool done = false;
@@ -909,6 +923,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
 
   __shared__ int sh_int[SEL_WARPS + 1];
   __shared__ float sh_f[SEL_WARPS + 1];
+  __shared__ MaxPair sh_mp[SEL_WARPS + 1];
   __shared__ Acc256 sh_acc[SEL_WARPS + 1];
   __shared__ unsigned long long sh_k[SEL_WARPS + 1];
   __shared__ double sh_d[SEL_WARPS + 1];
@@ -944,22 +959,18 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
     const int C = (S + NT - 1) / NT;
     const int j0 = min(S, tid * C), j1 = min(S, j0 + C);
     // the smallest nonzero survival: the sorted keys end with the zeros
-    // (key 1), so it sits just before the first of them (checked for the
-    // batches of the fast order only; larger ones span too many decades)
-    bool narrow = false;
-    if (S <= kFastMaxNK) {
-      if (tid == 0) sh_int[SEL_WARPS] = e_max;
-      __syncthreads();
-      for (int j = j0; j < j1; ++j) {
-        if (keys[j] != 1ull && (j + 1 == S || keys[j + 1] == 1ull)) {
-          const int ex = static_cast<int>(((keys[j] - 1ull) >> 52) & 0x7FF);
-          sh_int[SEL_WARPS] = ex == 0 ? 1 : ex;
-        }
+    // (key 1), so it sits just before the first of them
+    if (tid == 0) sh_int[SEL_WARPS] = e_max;
+    __syncthreads();
+    for (int j = j0; j < j1; ++j) {
+      if (keys[j] != 1ull && (j + 1 == S || keys[j + 1] == 1ull)) {
+        const int ex = static_cast<int>(((keys[j] - 1ull) >> 52) & 0x7FF);
+        sh_int[SEL_WARPS] = ex == 0 ? 1 : ex;
       }
-      __syncthreads();
-      narrow = sh_int[SEL_WARPS] >= e_max - kFixG128;
-      __syncthreads();
     }
+    __syncthreads();
+    const bool narrow = sh_int[SEL_WARPS] >= e_max - kFixG128;
+    __syncthreads();
     if (narrow) {
       Acc128 tot = {0ull, 0ull};
       for (int j = j0; j < j1; ++j) acc128_add(tot, to_fixed128(key_value(keys[j]), e_max));
@@ -1014,14 +1025,15 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
       float cf[kMaxChunk + 1];  // forced cost at b0 .. b1 (inclusive)
       const int cnt = (b1 - b0) + (has_next ? 1 : 0);
       if (mode == 1) {
-        float pre = -INFINITY;
-        for (int i = tid; i < T; i += NT) pre = fmax_nan(pre, a.cost[i]);
-        pre = block_reduce(pre, OpMaxNan(), -INFINITY, sh_f);
-        float loc = -INFINITY;
-        for (int b = b0; b < b1; ++b) loc = fmax_nan(loc, cost[b]);
-        float run = block_excl_scan(loc, OpMaxNan(), -INFINITY, sh_f,
-                                    static_cast<float *>(nullptr));
-        run = fmax_nan(run, pre);
+        // one scan for both: the maximum of cost[0 .. T) (its total) and
+        // the running maximum of the chunks before this thread's
+        MaxPair v{-INFINITY, -INFINITY};
+        for (int i = tid; i < T; i += NT) v.pre = fmax_nan(v.pre, a.cost[i]);
+        for (int b = b0; b < b1; ++b) v.run = fmax_nan(v.run, cost[b]);
+        MaxPair tot;
+        const MaxPair ex = block_excl_scan(v, OpMaxPair(), MaxPair{-INFINITY, -INFINITY},
+                                           sh_mp, &tot);
+        float run = fmax_nan(ex.run, tot.pre);
         for (int i = 0; i < cnt; ++i) {
           run = fmax_nan(run, cost[b0 + i]);
           cf[i] = run;
@@ -1064,7 +1076,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1)
       for (int i = 0; i < cnt; ++i) {
         const float den32 = cf[i] + a.draft_cost;
         if (!(den32 > 0.0f)) st |= DSPARK_DEV_COST_NONPOS;
-        const float num32 = static_cast<float>(Pl[i]) + static_cast<float>(n_s);
+        const float num32 = f64_to_f32_rn(Pl[i]) + static_cast<float>(n_s);
         fa[i] = __fdiv_rn(num32, den32);
         fast = fast && den32 >= 1.17549435e-38f && isfinite(fa[i]);
         if (i < b1 - b0) amax = fmaxf(amax, fa[i]);

@@ -191,7 +191,7 @@ def test_survivals_equal_in_fp32_but_not_in_fp64():
     r = _both(conf, None, cost, 2)
     assert r["order"].tolist() == [2, 3, 0, 1]
     rng = np.random.default_rng(99)
-    for N, K in ((300, 6), (256, 7), (600, 6)):
+    for N, K in ((300, 6), (256, 7), (600, 6), (1200, 6), (1500, 6)):
         ulps = rng.integers(0, 6, (N, K))
         conf = (1.0 - ulps * 2.0 ** -24).astype(np.float32)
         conf[rng.uniform(size=(N, K)) < 0.3] = np.float32(0.5)
@@ -199,13 +199,58 @@ def test_survivals_equal_in_fp32_but_not_in_fp64():
         _both(conf, None, cost, N)
 
 
+def test_survival_products_through_the_subnormal_range():
+    """Products that round inside the fp64 subnormal range and underflow to
+    zero, fp32 subnormal confidences, and survivals whose fp32 copies are
+    fp32 subnormals: survivals, order, sums and selection equal the
+    oracle's bit for bit (the products are IEEE multiplies rounded to
+    nearest even, the copies IEEE conversions), in a batch of 3072 slots
+    and one of 6144 (the kernel converts between fp32 and fp64 on the fp64
+    pipe below 4096 slots and in integer arithmetic from there)."""
+    rng = np.random.default_rng(31)
+    K = 32
+    for N in (96, 192):
+        m = N // 3
+        conf = rng.uniform(0.5, 1.0, (N, K)).astype(np.float32)
+        # 2^-1008 after eight factors, then down through the subnormals
+        # (2^-1022 .. 2^-1074) with rounding at every step
+        conf[:m, :8] = np.float32(2.0 ** -126)
+        conf[:m, 8:] = (2.0 ** rng.uniform(-12, 0, (m, K - 8))).astype(np.float32)
+        # an fp32 subnormal first factor
+        sub = rng.integers(1, 1 << 23, m).astype(np.uint32).view(np.float32)
+        conf[m:2 * m, 0] = sub
+        conf[m:2 * m, 1:] = rng.uniform(0.01, 1.0, (m, K - 1)).astype(np.float32)
+        # survivals near 2^-140, whose fp32 copies are subnormal
+        conf[2 * m:, 0] = (2.0 ** -60 * rng.uniform(1, 2, N - 2 * m)).astype(np.float32)
+        conf[2 * m:, 1] = (2.0 ** -80 * rng.uniform(1, 2, N - 2 * m)).astype(np.float32)
+        conf[2 * m:, 2:] = rng.uniform(0.3, 1.0, (N - 2 * m, K - 2)).astype(np.float32)
+        # the cases are reached: fp64 subnormal products, products that
+        # underflow to zero, and fp32 subnormal copies
+        p = np.asarray(oracle.survival(conf, None)[0], np.float64)
+        assert np.any((p > 0) & (p < 2.0 ** -1022)) and np.any(p == 0)
+        f = p.astype(np.float32)
+        assert np.any((f > 0) & (f < np.float32(2.0 ** -126)))
+        cost = (5 + 0.001 * np.arange(N * K + 8)).astype(np.float32)
+        _both(conf, None, cost, 1)
+
+
 def test_tiny_survivals_exact_sums():
-    """Survivals spanning hundreds of binary orders of magnitude."""
+    """Survivals spanning hundreds of binary orders of magnitude (the wide
+    fixed-point sums), in a small batch and in one of 15360 slots; and a
+    batch of that size within 2^61 of its largest survival (the narrow
+    sums)."""
     rng = np.random.default_rng(8)
     conf = rng.uniform(0, 1, (64, 32)).astype(np.float32) ** 8
     conf[:4, :] = 1e-30
     cost = (5 + 0.001 * np.arange(4096)).astype(np.float32)
     _both(conf, None, cost, 1)
+    cost = (5 + 0.001 * np.arange(16384)).astype(np.float32)
+    for power, wide in ((6.0, True), (0.25, False)):
+        conf = rng.uniform(0, 1, (1024, 15)).astype(np.float32) ** power
+        p = np.asarray(oracle.survival(conf, None)[0], np.float64)
+        nz = p[p > 0]
+        assert (nz.min() < nz.max() * 2.0 ** -61) == wide
+        _both(conf, None, cost, 1)
 
 
 def test_scheduler_alongside_chain_then_gather():
