@@ -204,7 +204,7 @@ DSPARK_API dspark_status dspark_chain_lmhead(
  * process exits.  The first call on each device looks up the array's device
  * address with cudaGetSymbolAddress (that device must be current), and so
  * does the first call after the device's context was replaced (for example
- * by cudaDeviceReset); make that first call before any stream capture.
+ * by cudaDeviceReset).
  * Every call shares the one array and keeps the last call's contents (each
  * call clears what must start at zero), so calls that overlap on the GPU
  * race: order them on one stream or with events.

@@ -15,13 +15,12 @@
 // array's name as a device address: its device address is queried with
 // cudaGetSymbolAddress, with that device current, by the first call made on
 // that device (and again by the first call after the device's context was
-// replaced, e.g. by cudaDeviceReset).  That first call should therefore come
-// before any stream capture.  All calls share the one array and each call
-// leaves its contents behind; the parts that must start at zero are cleared
-// at the start of every call (the chain launch clears the per-call state,
-// this file clears the status word).  Calls that overlap on the GPU would
-// race on the array, so they must be ordered (one stream, or explicit
-// events).
+// replaced, e.g. by cudaDeviceReset).  All calls share the one array and
+// each call leaves its contents behind; the parts that must start at zero
+// are cleared at the start of every call (the chain launch clears the
+// per-call state, this file clears the status word).  Calls that overlap on
+// the GPU would race on the array, so they must be ordered (one stream, or
+// explicit events).
 //
 // Every argument check runs before the first CUDA call, so a rejected call
 // enqueues nothing.
