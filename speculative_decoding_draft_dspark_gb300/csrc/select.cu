@@ -290,7 +290,8 @@ __device__ __forceinline__ double f32_to_f64(float c) {
 
 // d rounded to the nearest float, for d a non-negative double below 2^127
 __device__ __forceinline__ float f64_to_f32_rn(double d) {
-  const unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(d));
+  const unsigned long long b =
+      static_cast<unsigned long long>(__double_as_longlong(d));
   const int e = static_cast<int>(b >> 52);  // sign 0
   if (e == 0) return 0.0f;  // fp64 subnormals lie far below half an fp32 one
   const unsigned long long m = (b & ((1ull << 52) - 1ull)) | (1ull << 52);
@@ -303,8 +304,9 @@ __device__ __forceinline__ float f64_to_f32_rn(double d) {
   if (round && (sticky || (q & 1ull))) q += 1ull;
   // normal: q in [2^23, 2^24], a carry lands in the exponent (up to 2^127
   // at most); subnormal: q below 2^23, or 2^23 for the smallest normal
-  const uint32_t bits = e32 >= 1 ? (static_cast<uint32_t>(e32 - 1) << 23) + static_cast<uint32_t>(q)
-                                 : static_cast<uint32_t>(q);
+  const uint32_t bits = e32 >= 1
+                            ? (static_cast<uint32_t>(e32 - 1) << 23) + static_cast<uint32_t>(q)
+                            : static_cast<uint32_t>(q);
   return __uint_as_float(bits);
 }
 
